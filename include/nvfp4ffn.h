@@ -1,0 +1,204 @@
+/*
+ * nvfp4ffn.h -- C ABI of libnvfp4ffn.so: NVFP4 weight-only SwiGLU FFN decode
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ *   out[M, H] = down( act( gate(x) ) * up(x) ),   M = 1..16,
+ *   x, out BF16;  gate [I, H], up [I, H], down [H, I] NVFP4;  act = SiLU | GeLU-tanh.
+ *
+ * What the calls restate (Atlas engine pages):
+ *  - "spark_model/layers/dense_ffn.rs", module doc comment: the dense SwiGLU
+ *    FFN, gate = gate_proj(x), up = up_proj(x), out = down_proj(SiLU(gate)*up),
+ *    decoded with the weights dequantised inside the dot product.
+ *  - same page, doc comment of DenseFfnLayer::ensure_int8_weight: an NVFP4
+ *    projection is packed E2M1 codes [N, K/2], one E4M3 scale per 16 K
+ *    elements [N, K/16], and one FP32 `weight_scale_2` per tensor.
+ *  - same page, DenseFfnLayer::forward: the decode FFN as a dual gate+up GEMV
+ *    followed by the activation and a down GEMV; forward_km / forward_k2 /
+ *    forward_k3: the same for M verify rows, each weight read once for all M.
+ *  - same page, DenseFfnLayer::ensure_nvfp4_mmq_weight: a load-time repack of
+ *    the checkpoint NVFP4 into a kernel layout that is a raw bit shuffle of the
+ *    same codes and scale bytes.
+ *  - "spark_model/weight_loader/qwen35_dense.rs", load_layers: BF16/FP32
+ *    weights become NVFP4 at load time through a global-absmax kernel and a
+ *    quantize kernel (quantize_to_nvfp4).
+ *
+ * Conventions for every call:
+ *  - Pointers marked (device) are device pointers owned by the caller; the
+ *    library never frees them and keeps no reference after the call returns.
+ *  - Calls are asynchronous on `stream` unless marked "synchronises".
+ *  - The return value is a status; nothing aborts or throws across the ABI.
+ *    Argument errors are detected on the host before any launch; a failed
+ *    launch is reported as NVFP4_ERR_CUDA with the CUDA error left readable
+ *    through cudaGetLastError().
+ *  - BF16 tensors are row-major with a row stride equal to their width.
+ *  - Device pointers must be 16-byte aligned.
+ */
+#ifndef NVFP4FFN_H
+#define NVFP4FFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_NULL = 1,      /* a required pointer is NULL */
+    NVFP4_ERR_SHAPE = 2,     /* a size is <= 0, or K/H/I is not a multiple of 16 */
+    NVFP4_ERR_ALIGN = 3,     /* a device pointer is not 16-byte aligned */
+    NVFP4_ERR_RANGE = 4,     /* M outside [1, 16], or an unknown enum value */
+    NVFP4_ERR_WORKSPACE = 5, /* workspace smaller than the size query returns */
+    NVFP4_ERR_CUDA = 6,      /* a CUDA runtime call or launch failed */
+    NVFP4_ERR_TIMEOUT = 7,   /* a kernel gave up on a bounded wait (device status word) */
+    NVFP4_ERR_ALIAS = 8      /* input and output buffers overlap */
+} nvfp4_status;
+
+/* Gating nonlinearity (enum FfnActivation on the dense-FFN page).
+ * SiLU(t) = t / (1 + e^-t); GeLU-tanh(t) = 0.5 t (1 + tanh(sqrt(2/pi)(t + 0.044715 t^3))). */
+typedef enum { NVFP4_ACT_SILU = 0, NVFP4_ACT_GELU_TANH = 1 } nvfp4_act;
+
+/* Element type of the weight handed to nvfp4_quantize. */
+typedef enum { NVFP4_SRC_F32 = 0, NVFP4_SRC_BF16 = 1 } nvfp4_src_dtype;
+
+/* ------------------------------------------------------------------ quantise */
+
+/* Bytes of scratch nvfp4_quantize needs (a few words; independent of N, K). */
+size_t nvfp4_quantize_scratch_bytes(int N, int K);
+
+/*
+ * Quantise a weight W [N, K] (row-major, fp32 or bf16, device) to NVFP4 in the
+ * canonical checkpoint layout ("spark_model/weight_loader/qwen35_dense.rs",
+ * load_layers: global absmax, then quantize):
+ *   amax   = max |W|;  scale2 = amax / 2688 (= 6 * 448), or 1 when amax == 0
+ *   per 16-element block b of a row:  s_b = E4M3(bamax_b / 6 / scale2)
+ *   per element:  code = E2M1(w / (E4M3value(s_b) * scale2))   (code 0 with
+ *   the element's sign when s_b == 0)
+ * in IEEE fp32 with that operation order; both conversions round to nearest,
+ * ties to even, saturate at the largest finite value and keep the sign.
+ *   codes  (device, out) u8 [N, K/2]: element 2j in the low nibble of byte j.
+ *   scales (device, out) u8 [N, K/16]: E4M3 ("fn": bias 7, max 448).
+ *   scale2_out (host, out): the per-tensor FP32 scale.  A device copy is left
+ *   at byte offset 4 of `scratch`.
+ *   scratch (device) >= nvfp4_quantize_scratch_bytes(N, K).
+ * Requirements: N >= 1, K >= 16, K % 16 == 0, W finite.
+ * Synchronises `stream` (it reads scale2 back to the host): a load-time call.
+ */
+nvfp4_status nvfp4_quantize(const void* w, nvfp4_src_dtype dtype, int N, int K,
+                            uint8_t* codes, uint8_t* scales, float* scale2_out,
+                            void* scratch, size_t scratch_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ repack */
+
+/*
+ * Kernel layout ("fragment layout"): a byte permutation of the canonical codes
+ * and scales (the principle of DenseFfnLayer::ensure_nvfp4_mmq_weight: same
+ * codes, same scale bytes, no numerics), zero-padded to N' = roundup(N, 128)
+ * rows and K' = roundup(K, 64) columns.  For N % 128 == 0 and K % 64 == 0 it
+ * holds exactly the canonical byte count N*K*9/16.  The layout is opaque to
+ * callers; nvfp4_unpack inverts it.
+ */
+size_t nvfp4_repacked_bytes(int N, int K);
+
+/* codes [N, K/2], scales [N, K/16] (device, canonical) -> packed (device,
+ * nvfp4_repacked_bytes(N, K) bytes).  N >= 1, K % 16 == 0. */
+nvfp4_status nvfp4_repack(const uint8_t* codes, const uint8_t* scales, int N, int K,
+                          void* packed, cudaStream_t stream);
+
+/* Gate and up projections ([I, H] each) interleaved so that one kernel reads
+ * gate row n and up row n together: 2 * nvfp4_repacked_bytes(I, H) bytes. */
+size_t nvfp4_repacked_gate_up_bytes(int I, int H);
+nvfp4_status nvfp4_repack_gate_up(const uint8_t* gate_codes, const uint8_t* gate_scales,
+                                  const uint8_t* up_codes, const uint8_t* up_scales,
+                                  int I, int H, void* packed, cudaStream_t stream);
+
+/* Inverse of nvfp4_repack (a test and inspection aid): packed -> canonical
+ * codes [N, K/2] and scales [N, K/16] (device). */
+nvfp4_status nvfp4_unpack(const void* packed, int N, int K, uint8_t* codes,
+                          uint8_t* scales, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ GEMV */
+
+/*
+ * Workspace bytes for nvfp4_gemv on the current device (cross-CTA partial
+ * sums and their counters).  The workspace must be zero-filled once after it
+ * is allocated (cudaMemset or nvfp4_workspace_init); every successful call
+ * leaves it ready for the next one.
+ */
+size_t nvfp4_gemv_workspace_bytes(int M, int N, int K);
+
+/*
+ * One NVFP4 projection (the w4a16 decode GEMV of "spark_model/layers/
+ * dense_ffn.rs", DenseFfnLayer::forward / forward_km):
+ *   y[m, n] = bf16( scale2 * sum_k x[m, k] * E2M1(c[n, k]) * E4M3(s[n, k/16]) )
+ *   x (device) bf16 [M, K];  packed_w (device) from nvfp4_repack(N, K);
+ *   y (device, out) bf16 [M, N];  ws (device) >= nvfp4_gemv_workspace_bytes.
+ * Requirements: 1 <= M <= 16, N >= 1, K >= 16, K % 16 == 0, x and y disjoint.
+ * Accumulation is fp32 on exactly dequantised weights; every x row is scaled
+ * by a power of two into the fp16 operand range, so any finite bf16 x works.
+ */
+nvfp4_status nvfp4_gemv(const void* x, int M, int K, const void* packed_w, float scale2,
+                        int N, void* y, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ FFN */
+
+/* Workspace bytes for ffn_swiglu_nvfp4 on the current device: the bf16
+ * activation h [M, I] plus the partial sums of both kernels.  Zero-fill once
+ * after allocation, as for nvfp4_gemv. */
+size_t ffn_swiglu_nvfp4_workspace_bytes(int M, int H, int I);
+
+/*
+ * The decode FFN (DenseFfnLayer::forward and forward_km on the dense-FFN
+ * page), in two launches:
+ *   1. g = bf16(gate_scale2 * gate.x),  u = bf16(up_scale2 * up.x),
+ *      h = bf16(act(g) * u)                      [M, I] bf16, in ws
+ *   2. out = bf16(down_scale2 * down.h)          [M, H] bf16
+ *   x (device) bf16 [M, H];  gate_up_packed (device) from
+ *   nvfp4_repack_gate_up(I, H);  down_packed (device) from nvfp4_repack(H, I);
+ *   out (device, out) bf16 [M, H];  ws (device) >= ffn_swiglu_nvfp4_workspace_bytes.
+ * Requirements: 1 <= M <= 16, H and I >= 16 and multiples of 16, x and out
+ * disjoint, act a nvfp4_act value.
+ */
+nvfp4_status ffn_swiglu_nvfp4(const void* x, int M, int H, int I,
+                              const void* gate_up_packed, float gate_scale2, float up_scale2,
+                              const void* down_packed, float down_scale2, nvfp4_act act,
+                              void* out, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Workspace bytes for ffn_gate_up_nvfp4 on the current device (zero-fill once). */
+size_t ffn_gate_up_nvfp4_workspace_bytes(int M, int H, int I);
+
+/*
+ * The gate/up half of the FFN alone (step 1 of ffn_swiglu_nvfp4; the fused
+ * dual GEMV + activation of DenseFfnLayer::forward on the dense-FFN page):
+ *   h[m, i] = bf16( act(bf16(gate_scale2 * gate.x)) * bf16(up_scale2 * up.x) )
+ *   x (device) bf16 [M, H];  gate_up_packed (device) from nvfp4_repack_gate_up;
+ *   h (device, out) bf16 [M, I];  ws (device) >= ffn_gate_up_nvfp4_workspace_bytes.
+ * A caller that adds its own terms to h (an adapter) finishes the layer with
+ * nvfp4_gemv on the down projection.  Requirements as for ffn_swiglu_nvfp4.
+ */
+nvfp4_status ffn_gate_up_nvfp4(const void* x, int M, int H, int I, const void* gate_up_packed,
+                               float gate_scale2, float up_scale2, nvfp4_act act, void* h,
+                               void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ utilities */
+
+/* Zero-fill a workspace (asynchronous memset on `stream`). */
+nvfp4_status nvfp4_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word at the
+ * start of a GEMV/FFN workspace: NVFP4_OK, or NVFP4_ERR_TIMEOUT when a kernel
+ * abandoned a bounded wait since the last check.
+ */
+nvfp4_status nvfp4_workspace_status(void* ws, cudaStream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* nvfp4_status_string(nvfp4_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4FFN_H */

@@ -1,0 +1,233 @@
+// api.cu -- the C ABI declared in include/nvfp4ffn.h: host-side argument
+// validation, workspace carving and launch of the sm_103a kernels.  No
+// arithmetic of the method lives here.
+#include <cstdint>
+#include <cstring>
+
+#include "internal.h"
+#include "layout.h"
+#include "nvfp4ffn.h"
+
+namespace {
+
+constexpr size_t kQuantizeScratch = 256;
+// Size assumed for workspace queries when no device is visible.
+constexpr int kFallbackSms = 160;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+int sms_for_sizing() {
+    const int n = nvf::device_sm_count();
+    return n > 0 ? n : kFallbackSms;
+}
+
+nvfp4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
+
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+// FFN workspace: [status][h (M x I bf16)][dual-kernel scratch][down-kernel scratch]
+struct FfnLayout {
+    size_t h_off, dual_off, dual_bytes, down_off, down_bytes, total;
+};
+
+FfnLayout ffn_layout(int M, int H, int I, int sms) {
+    FfnLayout l;
+    l.h_off = nvf::kStatusBytes;
+    l.dual_off = l.h_off + round256((size_t)M * I * 2);
+    l.dual_bytes = round256(nvf::gemv_scratch_bytes(2, M, I, H, sms));
+    l.down_off = l.dual_off + l.dual_bytes;
+    l.down_bytes = round256(nvf::gemv_scratch_bytes(1, M, H, I, sms));
+    l.total = l.down_off + l.down_bytes;
+    return l;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t nvfp4_quantize_scratch_bytes(int N, int K) {
+    (void)N;
+    (void)K;
+    return kQuantizeScratch;
+}
+
+nvfp4_status nvfp4_quantize(const void* w, nvfp4_src_dtype dtype, int N, int K, uint8_t* codes,
+                            uint8_t* scales, float* scale2_out, void* scratch,
+                            size_t scratch_bytes, cudaStream_t stream) {
+    if (!w || !codes || !scales || !scale2_out || !scratch) return NVFP4_ERR_NULL;
+    if (dtype != NVFP4_SRC_F32 && dtype != NVFP4_SRC_BF16) return NVFP4_ERR_RANGE;
+    if (N < 1 || K < 16 || K % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (!aligned16(w) || !aligned16(codes) || !aligned16(scratch)) return NVFP4_ERR_ALIGN;
+    if (scratch_bytes < kQuantizeScratch) return NVFP4_ERR_WORKSPACE;
+    cudaError_t e = nvf::launch_quantize(w, dtype == NVFP4_SRC_BF16 ? 1 : 0, N, K, codes, scales,
+                                         scratch, stream);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    float s2 = 0.0f;
+    e = cudaMemcpyAsync(&s2, reinterpret_cast<char*>(scratch) + 4, 4, cudaMemcpyDeviceToHost,
+                        stream);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    *scale2_out = s2;
+    return NVFP4_OK;
+}
+
+size_t nvfp4_repacked_bytes(int N, int K) {
+    if (N < 1 || K < 16) return 0;
+    return nvf::repacked_bytes(N, K, 1);
+}
+
+size_t nvfp4_repacked_gate_up_bytes(int I, int H) {
+    if (I < 1 || H < 16) return 0;
+    return nvf::repacked_bytes(I, H, 2);
+}
+
+nvfp4_status nvfp4_repack(const uint8_t* codes, const uint8_t* scales, int N, int K, void* packed,
+                          cudaStream_t stream) {
+    if (!codes || !scales || !packed) return NVFP4_ERR_NULL;
+    if (N < 1 || K < 16 || K % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (!aligned16(packed)) return NVFP4_ERR_ALIGN;
+    return cuda_status(
+        nvf::launch_repack(codes, scales, N, K, reinterpret_cast<uint8_t*>(packed), 1, 0, stream));
+}
+
+nvfp4_status nvfp4_repack_gate_up(const uint8_t* gate_codes, const uint8_t* gate_scales,
+                                  const uint8_t* up_codes, const uint8_t* up_scales, int I, int H,
+                                  void* packed, cudaStream_t stream) {
+    if (!gate_codes || !gate_scales || !up_codes || !up_scales || !packed) return NVFP4_ERR_NULL;
+    if (I < 1 || H < 16 || H % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (!aligned16(packed)) return NVFP4_ERR_ALIGN;
+    uint8_t* p = reinterpret_cast<uint8_t*>(packed);
+    cudaError_t e = nvf::launch_repack(gate_codes, gate_scales, I, H, p, 2, 0, stream);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    return cuda_status(nvf::launch_repack(up_codes, up_scales, I, H, p, 2, 1, stream));
+}
+
+nvfp4_status nvfp4_unpack(const void* packed, int N, int K, uint8_t* codes, uint8_t* scales,
+                          cudaStream_t stream) {
+    if (!packed || !codes || !scales) return NVFP4_ERR_NULL;
+    if (N < 1 || K < 16 || K % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (!aligned16(packed)) return NVFP4_ERR_ALIGN;
+    return cuda_status(nvf::launch_unpack(reinterpret_cast<const uint8_t*>(packed), N, K, codes,
+                                          scales, stream));
+}
+
+size_t nvfp4_gemv_workspace_bytes(int M, int N, int K) {
+    if (M < 1 || M > 16 || N < 1 || K < 16) return 0;
+    return nvf::kStatusBytes + round256(nvf::gemv_scratch_bytes(1, M, N, K, sms_for_sizing()));
+}
+
+nvfp4_status nvfp4_gemv(const void* x, int M, int K, const void* packed_w, float scale2, int N,
+                        void* y, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!x || !packed_w || !y || !ws) return NVFP4_ERR_NULL;
+    if (M < 1 || M > 16) return NVFP4_ERR_RANGE;
+    if (N < 1 || K < 16 || K % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(packed_w) || !aligned16(y) || !aligned16(ws))
+        return NVFP4_ERR_ALIGN;
+    if (overlap(x, (size_t)M * K * 2, y, (size_t)M * N * 2)) return NVFP4_ERR_ALIAS;
+    const int sms = nvf::device_sm_count();
+    if (sms <= 0) return NVFP4_ERR_CUDA;
+    const size_t need = nvf::kStatusBytes + round256(nvf::gemv_scratch_bytes(1, M, N, K, sms));
+    if (ws_bytes < need) return NVFP4_ERR_WORKSPACE;
+    char* w = reinterpret_cast<char*>(ws);
+    return cuda_status(nvf::launch_stream_gemv(1, x, M, K, packed_w, N, scale2, scale2, 0, y,
+                                               reinterpret_cast<int*>(w), w + nvf::kStatusBytes,
+                                               need - nvf::kStatusBytes, sms, stream));
+}
+
+size_t ffn_swiglu_nvfp4_workspace_bytes(int M, int H, int I) {
+    if (M < 1 || M > 16 || H < 16 || I < 16) return 0;
+    return ffn_layout(M, H, I, sms_for_sizing()).total;
+}
+
+nvfp4_status ffn_swiglu_nvfp4(const void* x, int M, int H, int I, const void* gate_up_packed,
+                              float gate_scale2, float up_scale2, const void* down_packed,
+                              float down_scale2, nvfp4_act act, void* out, void* ws,
+                              size_t ws_bytes, cudaStream_t stream) {
+    if (!x || !gate_up_packed || !down_packed || !out || !ws) return NVFP4_ERR_NULL;
+    if (M < 1 || M > 16) return NVFP4_ERR_RANGE;
+    if (act != NVFP4_ACT_SILU && act != NVFP4_ACT_GELU_TANH) return NVFP4_ERR_RANGE;
+    if (H < 16 || I < 16 || H % 16 != 0 || I % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(gate_up_packed) || !aligned16(down_packed) ||
+        !aligned16(out) || !aligned16(ws))
+        return NVFP4_ERR_ALIGN;
+    if (overlap(x, (size_t)M * H * 2, out, (size_t)M * H * 2)) return NVFP4_ERR_ALIAS;
+    const int sms = nvf::device_sm_count();
+    if (sms <= 0) return NVFP4_ERR_CUDA;
+    const FfnLayout l = ffn_layout(M, H, I, sms);
+    if (ws_bytes < l.total) return NVFP4_ERR_WORKSPACE;
+    char* w = reinterpret_cast<char*>(ws);
+    int* status = reinterpret_cast<int*>(w);
+    void* h = w + l.h_off;
+    cudaError_t e = nvf::launch_stream_gemv(2, x, M, H, gate_up_packed, I, gate_scale2, up_scale2,
+                                            (int)act, h, status, w + l.dual_off, l.dual_bytes, sms,
+                                            stream);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    e = nvf::launch_stream_gemv(1, h, M, I, down_packed, H, down_scale2, down_scale2, 0, out,
+                                status, w + l.down_off, l.down_bytes, sms, stream);
+    return cuda_status(e);
+}
+
+size_t ffn_gate_up_nvfp4_workspace_bytes(int M, int H, int I) {
+    if (M < 1 || M > 16 || H < 16 || I < 16) return 0;
+    return nvf::kStatusBytes + round256(nvf::gemv_scratch_bytes(2, M, I, H, sms_for_sizing()));
+}
+
+nvfp4_status ffn_gate_up_nvfp4(const void* x, int M, int H, int I, const void* gate_up_packed,
+                               float gate_scale2, float up_scale2, nvfp4_act act, void* h,
+                               void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!x || !gate_up_packed || !h || !ws) return NVFP4_ERR_NULL;
+    if (M < 1 || M > 16) return NVFP4_ERR_RANGE;
+    if (act != NVFP4_ACT_SILU && act != NVFP4_ACT_GELU_TANH) return NVFP4_ERR_RANGE;
+    if (H < 16 || I < 16 || H % 16 != 0 || I % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(gate_up_packed) || !aligned16(h) || !aligned16(ws))
+        return NVFP4_ERR_ALIGN;
+    if (overlap(x, (size_t)M * H * 2, h, (size_t)M * I * 2)) return NVFP4_ERR_ALIAS;
+    const int sms = nvf::device_sm_count();
+    if (sms <= 0) return NVFP4_ERR_CUDA;
+    const size_t need = nvf::kStatusBytes + round256(nvf::gemv_scratch_bytes(2, M, I, H, sms));
+    if (ws_bytes < need) return NVFP4_ERR_WORKSPACE;
+    char* w = reinterpret_cast<char*>(ws);
+    return cuda_status(nvf::launch_stream_gemv(2, x, M, H, gate_up_packed, I, gate_scale2,
+                                               up_scale2, (int)act, h, reinterpret_cast<int*>(w),
+                                               w + nvf::kStatusBytes, need - nvf::kStatusBytes,
+                                               sms, stream));
+}
+
+nvfp4_status nvfp4_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!ws) return NVFP4_ERR_NULL;
+    return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, stream));
+}
+
+nvfp4_status nvfp4_workspace_status(void* ws, cudaStream_t stream) {
+    if (!ws) return NVFP4_ERR_NULL;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    int st = 0;
+    if (cudaMemcpy(&st, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    if (st == 0) return NVFP4_OK;
+    if (cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return NVFP4_ERR_CUDA;
+    return NVFP4_ERR_TIMEOUT;
+}
+
+const char* nvfp4_status_string(nvfp4_status status) {
+    switch (status) {
+        case NVFP4_OK: return "ok";
+        case NVFP4_ERR_NULL: return "null pointer argument";
+        case NVFP4_ERR_SHAPE: return "invalid shape (sizes must be positive, K/H/I multiples of 16)";
+        case NVFP4_ERR_ALIGN: return "device pointer not 16-byte aligned";
+        case NVFP4_ERR_RANGE: return "argument out of range (M must be 1..16; enum value unknown)";
+        case NVFP4_ERR_WORKSPACE: return "workspace too small";
+        case NVFP4_ERR_CUDA: return "CUDA runtime error";
+        case NVFP4_ERR_TIMEOUT: return "kernel abandoned a bounded wait";
+        case NVFP4_ERR_ALIAS: return "input and output buffers overlap";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

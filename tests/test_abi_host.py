@@ -1,0 +1,113 @@
+"""The C ABI without a GPU: the library builds and loads, exports every symbol
+the header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from nvfp4_weight_only_gb300 import ffi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4ffn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return ffi.load(build_if_missing=True)
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_binding_exports():
+    assert header_functions() == sorted(ffi.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in ffi.STATUS_NAMES.items():
+        s = lib.nvfp4_status_string(code)
+        assert isinstance(s, bytes) and len(s) > 0, name
+    assert lib.nvfp4_status_string(99) == b"unknown status"
+
+
+def test_repacked_sizes(lib):
+    # aligned shapes keep the canonical byte count N*K*9/16
+    for N, K in ((5120, 17408), (17408, 5120), (4096, 4096), (128, 64)):
+        assert lib.nvfp4_repacked_bytes(N, K) == N * K * 9 // 16
+        assert lib.nvfp4_repacked_gate_up_bytes(N, K) == 2 * N * K * 9 // 16
+    # ragged shapes are zero-padded to 128 rows x 64 columns
+    assert lib.nvfp4_repacked_bytes(200, 272) == 256 * 320 * 9 // 16
+    assert lib.nvfp4_repacked_bytes(0, 64) == 0
+
+
+def test_workspace_queries_are_positive(lib):
+    for M in (1, 2, 8, 9, 16):
+        assert lib.nvfp4_gemv_workspace_bytes(M, 5120, 17408) > 256
+        assert lib.ffn_swiglu_nvfp4_workspace_bytes(M, 5120, 17408) > 256 + M * 17408 * 2
+    assert lib.nvfp4_gemv_workspace_bytes(0, 5120, 17408) == 0
+    assert lib.nvfp4_gemv_workspace_bytes(17, 5120, 17408) == 0
+    assert lib.nvfp4_quantize_scratch_bytes(5120, 17408) >= 8
+
+
+FAKE = ctypes.c_void_p(0x10000)      # 16-byte aligned, never dereferenced
+MISALIGNED = ctypes.c_void_p(0x10004)
+NULL = ctypes.c_void_p(0)
+S = ctypes.c_void_p(0)
+
+
+def test_gemv_validation(lib):
+    g = lib.nvfp4_gemv
+    assert g(NULL, 1, 64, FAKE, 1.0, 64, FAKE, FAKE, 1 << 20, S) == 1
+    assert g(FAKE, 0, 64, FAKE, 1.0, 64, FAKE, FAKE, 1 << 20, S) == 4
+    assert g(FAKE, 17, 64, FAKE, 1.0, 64, FAKE, FAKE, 1 << 20, S) == 4
+    assert g(FAKE, 1, 40, FAKE, 1.0, 64, FAKE, FAKE, 1 << 20, S) == 2
+    assert g(FAKE, 1, 64, FAKE, 1.0, 0, FAKE, FAKE, 1 << 20, S) == 2
+    assert g(MISALIGNED, 1, 64, FAKE, 1.0, 64, ctypes.c_void_p(0x20000), FAKE, 1 << 20, S) == 3
+    # x and y overlap
+    assert g(FAKE, 1, 64, ctypes.c_void_p(0x30000), 1.0, 64, ctypes.c_void_p(0x10020), FAKE,
+             1 << 20, S) == 8
+
+
+def test_ffn_validation(lib):
+    f = lib.ffn_swiglu_nvfp4
+    A = [ctypes.c_void_p(0x10000 * i) for i in range(1, 6)]
+    assert f(NULL, 1, 256, 512, A[1], 1.0, 1.0, A[2], 1.0, 0, A[3], A[4], 1 << 24, S) == 1
+    assert f(A[0], 0, 256, 512, A[1], 1.0, 1.0, A[2], 1.0, 0, A[3], A[4], 1 << 24, S) == 4
+    assert f(A[0], 1, 256, 512, A[1], 1.0, 1.0, A[2], 1.0, 2, A[3], A[4], 1 << 24, S) == 4
+    assert f(A[0], 1, 250, 512, A[1], 1.0, 1.0, A[2], 1.0, 0, A[3], A[4], 1 << 24, S) == 2
+    assert f(A[0], 1, 256, 500, A[1], 1.0, 1.0, A[2], 1.0, 0, A[3], A[4], 1 << 24, S) == 2
+    assert f(A[0], 1, 256, 512, MISALIGNED, 1.0, 1.0, A[2], 1.0, 0, A[3], A[4], 1 << 24, S) == 3
+    assert f(A[0], 1, 256, 512, A[1], 1.0, 1.0, A[2], 1.0, 0, A[0], A[4], 1 << 24, S) == 8
+
+
+def test_quantize_and_repack_validation(lib):
+    s2 = ctypes.c_float()
+    q = lib.nvfp4_quantize
+    assert q(NULL, 0, 16, 64, FAKE, FAKE, ctypes.byref(s2), FAKE, 256, S) == 1
+    assert q(FAKE, 3, 16, 64, FAKE, FAKE, ctypes.byref(s2), FAKE, 256, S) == 4
+    assert q(FAKE, 0, 16, 24, FAKE, FAKE, ctypes.byref(s2), FAKE, 256, S) == 2
+    assert q(FAKE, 0, 0, 64, FAKE, FAKE, ctypes.byref(s2), FAKE, 256, S) == 2
+    assert q(FAKE, 0, 16, 64, FAKE, FAKE, ctypes.byref(s2), FAKE, 4, S) == 5
+    assert lib.nvfp4_repack(NULL, FAKE, 16, 64, FAKE, S) == 1
+    assert lib.nvfp4_repack(FAKE, FAKE, 16, 40, FAKE, S) == 2
+    assert lib.nvfp4_repack(FAKE, FAKE, 16, 64, MISALIGNED, S) == 3
+    assert lib.nvfp4_repack_gate_up(FAKE, FAKE, FAKE, NULL, 16, 64, FAKE, S) == 1
+    assert lib.nvfp4_unpack(FAKE, 16, 8, FAKE, FAKE, S) == 2
+    assert lib.nvfp4_workspace_init(NULL, 16, S) == 1
+    assert lib.nvfp4_workspace_status(NULL, S) == 1
+
+
+def test_binding_raises_without_cuda_tensors():
+    import torch
+    with pytest.raises(ValueError):
+        ffi.nvfp4_gemv(torch.zeros(1, 64, dtype=torch.bfloat16), torch.zeros(10, dtype=torch.uint8),
+                       1.0, 64)
