@@ -23,7 +23,8 @@ constexpr size_t kStatusBytes = 256;
 size_t gemv_scratch_bytes(int streams, int M, int N, int K, int num_sms);
 cudaError_t launch_stream_gemv(int streams, const void* x, int M, int K, const void* packed, int N,
                                float scale_a, float scale_b, int act, void* out, int* status,
-                               void* scratch, size_t scratch_bytes, int num_sms, cudaStream_t s);
+                               void* scratch, size_t scratch_bytes, int num_sms, bool early_weights,
+                               cudaStream_t s);
 
 int device_sm_count();
 

@@ -13,12 +13,12 @@
 //            i.e. exactly the A-fragment registers a0..a3 of block j.
 //   scales : byte 8g + 2j + (r&1) holds the E4M3 scale of row g + 8*(r&1),
 //            block j.
-//   row block = 8 units of consecutive 16-row tiles (128 rows), for one chunk;
+//   row block = 16 units of consecutive 16-row tiles (256 rows), for one chunk;
 //   order  = [row block][chunk][tile in block], so one row block's data for
 //            a run of chunks is one contiguous byte range.
 //
-// Rows are zero-padded to a multiple of 128 and K to a multiple of 64 (zero
-// codes with zero scales contribute nothing).  The gate/up variant stores the
+// Rows are zero-padded to a multiple of 256 and K to a multiple of 256 (four
+// chunks; zero codes with zero scales contribute nothing).  The gate/up variant stores the
 // gate unit and the up unit of the same tile back to back (1152 bytes), so the
 // dual kernel streams both projections of its rows from one range.
 #pragma once
@@ -28,9 +28,10 @@
 namespace nvf {
 
 constexpr int kTileRows = 16;
-constexpr int kBlockTiles = 8;
-constexpr int kBlockRows = kTileRows * kBlockTiles;  // 128
+constexpr int kBlockTiles = 16;
+constexpr int kBlockRows = kTileRows * kBlockTiles;  // 256
 constexpr int kChunkK = 64;
+constexpr int kChunkAlign = 4;  // chunks per row block are a multiple of this
 constexpr int kUnitCodeBytes = 512;
 constexpr int kUnitScaleBytes = 64;
 constexpr int kUnitBytes = kUnitCodeBytes + kUnitScaleBytes;  // 576
@@ -39,8 +40,8 @@ inline __host__ __device__ long long ceil_div(long long a, long long b) { return
 
 struct Geometry {
     int N, K;    // logical rows, columns
-    int RB;      // row blocks of 128 rows
-    int C;       // chunks of 64 K elements
+    int RB;      // row blocks of 256 rows
+    int C;       // chunks of 64 K elements (a multiple of kChunkAlign)
 };
 
 inline __host__ __device__ Geometry geometry(int N, int K) {
@@ -48,7 +49,7 @@ inline __host__ __device__ Geometry geometry(int N, int K) {
     g.N = N;
     g.K = K;
     g.RB = (int)ceil_div(N, kBlockRows);
-    g.C = (int)ceil_div(K, kChunkK);
+    g.C = (int)(ceil_div(ceil_div(K, kChunkK), kChunkAlign) * kChunkAlign);
     return g;
 }
 

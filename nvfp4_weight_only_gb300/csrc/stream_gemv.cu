@@ -9,24 +9,24 @@
 // GEMV, activation, down GEMV; forward_km: each weight read once for all M
 // rows) is the prior art; the structure here is GB300's own:
 //
-//   * persistent grid, one CTA per SM: 8 consumer warps + 1 producer warp;
-//   * the producer streams contiguous runs of repacked weight units through a
-//     ring of shared-memory stages with the bulk-copy (TMA) engine, completion
-//     tracked by mbarriers;
-//   * each consumer warp owns one 16-row tile of every 128-row block and turns
-//     its 16 code bytes per 64-K chunk into exact f16 weights
-//     (E2M1 -> f16 by cvt, times the E4M3 scale by an exact f16 multiply) fed
-//     as the A operand of mma.sync m16n8k16 with fp32 accumulators; the token
-//     rows (x) are the B operand, staged once per CTA range in shared memory
-//     as f16 after a per-token power-of-two scaling (exact; keeps any finite
-//     bf16 input inside the f16 range);
-//   * work = (row block, chunk) steps in row-major order, split into equal
+//   * persistent grid, one CTA of 16 warps per SM; warp w owns the 16-row
+//     tile w of every 256-row block of the repacked weight (layout.h);
+//   * weights stream through a ring of shared-memory stages filled by the
+//     bulk-copy (TMA) engine, completion tracked by one mbarrier per stage;
+//     the last warp to finish with a stage refills it with the step that lies
+//     a full ring ahead, so no warp ever blocks to produce;
+//   * per k16 block a warp turns its 4 code bytes into exact f16 A fragments
+//     (one cvt per E2M1 pair), runs mma.sync m16n8k16 against the token rows
+//     (B operand, staged once per range in shared memory as f16 after an exact
+//     per-token power-of-two scaling that keeps any finite bf16 row inside the
+//     f16 range), and applies the two E4M3 row scales to the fp32 block sums;
+//   * work = (row block, step of chunks) in row-major order, split into equal
 //     contiguous ranges; a row block whose K range spans several ranges is
 //     finished by the last range to arrive (atomic counter), which sums the
 //     fp32 partial slots in range order, so results are deterministic.
 //
 // Every mbarrier wait is bounded (device status word + abort flag), and a CTA
-// drains its own bulk copies before it exits.
+// that gave up waits (bounded) for its own bulk copies before it exits.
 #include <cuda_bf16.h>
 
 #include "device_util.cuh"
@@ -35,24 +35,30 @@
 
 namespace nvf {
 
-constexpr int kConsumerWarps = kBlockTiles;  // one warp per 16-row tile
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;
+constexpr int kWarps = kBlockTiles;  // one warp per 16-row tile of a row block
+constexpr int kThreads = kWarps * 32;
 constexpr int kSmemMax = 227 * 1024;
 constexpr int kXBudget = 96 * 1024;
-constexpr int kRingBudget = 96 * 1024;
-constexpr int kMaxStages = 16;
+constexpr int kRingBudget = 200 * 1024;
+constexpr int kMaxStages = 8;
 constexpr int kMiscBytes = 512;
-constexpr int kConsumerBarrier = 1;
+// Chunks (of 64 K elements) summed in plain fp32 before the sum is folded into
+// the exact hi/lo pair.
+constexpr int kFoldChunks = 8;
+// Weight units (16 rows x 64 K) each warp handles per pipeline step; a step
+// spans kUnitsPerStep / streams chunks (a divisor of kChunkAlign).
+#ifndef NVF_UNITS_PER_STEP
+#define NVF_UNITS_PER_STEP 4
+#endif
+constexpr int kUnitsPerStep = NVF_UNITS_PER_STEP;
 
 struct Plan {
-    int NS, NT, G;
-    int RB, C, SRB;
-    long long L;
+    int NS, NT, RB, C, CS;  // CS: steps per row block
+    long long L;            // steps in the whole problem
     int grid, R;
-    long long Pmax;
-    int xcap, stage_bytes, stages, s_max, slot_floats;
-    int x_off, bar_off, misc_off;
+    long long Pmax;         // steps per range (max)
+    int cps, xcap, x_stride, stage_bytes, stages, s_max, slot_floats;
+    int x_off, bar_off, cnt_off, misc_off;
     size_t smem;
     size_t counters_off, partials_off, total;
 };
@@ -61,14 +67,16 @@ static Plan make_plan(int NS, int M, int N, int K, int num_sms) {
     Plan p{};
     p.NS = NS;
     p.NT = (M <= 8) ? 1 : 2;
-    p.G = (p.NT == 1) ? 1 : 2;
+    p.cps = kUnitsPerStep / NS;
     const Geometry g = geometry(N, K);
     p.RB = g.RB;
     p.C = g.C;
-    p.SRB = (int)ceil_div(p.RB, p.G);
-    p.L = (long long)p.SRB * p.C;
-    const int xchunk = p.NT * 1024;
-    const int xcap_max = kXBudget / xchunk;
+    p.CS = p.C / p.cps;
+    p.L = (long long)p.RB * p.CS;
+    // x lives in shared memory as f16, token-major: per token 128 bytes per
+    // chunk (+16 bytes of row padding that keeps the B-fragment loads free of
+    // bank conflicts).
+    const int xcap_max = (kXBudget - 16 * M) / (128 * M);
     p.grid = num_sms > 0 ? num_sms : 1;
     if (p.L < p.grid) p.grid = (int)p.L;
     for (int rpc = 1;; ++rpc) {
@@ -76,27 +84,29 @@ static Plan make_plan(int NS, int M, int N, int K, int num_sms) {
         if (R > p.L) R = p.L;
         p.R = (int)R;
         p.Pmax = ceil_div(p.L, p.R);
-        const long long need = p.Pmax < p.C ? p.Pmax : p.C;
+        const long long need = p.Pmax * p.cps < p.C ? p.Pmax * p.cps : p.C;
         if (need <= xcap_max || p.R == p.L) break;
     }
-    p.xcap = (int)(p.Pmax < p.C ? p.Pmax : p.C);
-    p.stage_bytes = p.G * kBlockTiles * kUnitBytes * NS;
-    const int x_bytes = p.xcap * xchunk;
-    int ring = kSmemMax - x_bytes - kMiscBytes - 16 * kMaxStages;
+    p.xcap = (int)(p.Pmax * p.cps < p.C ? p.Pmax * p.cps : p.C);
+    p.x_stride = p.xcap * 128 + 16;
+    p.stage_bytes = p.cps * kBlockTiles * kUnitBytes * NS;
+    const int x_bytes = M * p.x_stride;
+    int ring = kSmemMax - x_bytes - kMiscBytes - 32 * kMaxStages - 256;
     if (ring > kRingBudget) ring = kRingBudget;
     p.stages = ring / p.stage_bytes;
     if (p.stages > kMaxStages) p.stages = kMaxStages;
     if (p.stages < 2) p.stages = 2;
     p.x_off = (int)(ceil_div((long long)p.stages * p.stage_bytes, 128) * 128);
-    p.bar_off = p.x_off + x_bytes;
-    p.misc_off = p.bar_off + 16 * p.stages;
+    p.bar_off = (int)(ceil_div((long long)p.x_off + x_bytes, 16) * 16);
+    p.cnt_off = p.bar_off + 8 * p.stages;
+    p.misc_off = p.cnt_off + (int)(ceil_div(8LL * p.stages, 16) * 16);
     p.smem = (size_t)p.misc_off + kMiscBytes;
-    long long smax = ceil_div(p.Pmax, p.C) + 1;
-    if (smax > p.SRB) smax = p.SRB;
+    long long smax = ceil_div(p.Pmax, p.CS) + 1;
+    if (smax > p.RB) smax = p.RB;
     p.s_max = (int)smax;
-    p.slot_floats = p.G * kBlockTiles * NS * kTileRows * (p.NT * 8);
+    p.slot_floats = kBlockTiles * NS * kTileRows * (p.NT * 8);
     p.counters_off = 0;
-    p.partials_off = (size_t)ceil_div((long long)p.SRB * 4, 256) * 256;
+    p.partials_off = (size_t)ceil_div((long long)p.RB * kBlockTiles * 4, 256) * 256;
     p.total = p.partials_off + (size_t)p.R * p.s_max * p.slot_floats * sizeof(float);
     return p;
 }
@@ -109,29 +119,70 @@ struct KArgs {
     int* counters;
     int* status;
     long long L;
-    int M, K, N, C, RB, R, grid;
-    int stages, stage_bytes, x_off, bar_off, misc_off, s_max;
+    int M, K, N, C, CS, RB, R, grid;
+    int stages, stage_bytes, x_off, x_stride, bar_off, cnt_off, misc_off, s_max;
     float scale_a, scale_b;
     int act;
+    int early_weights;  // stream weights before waiting on the preceding kernel
 };
 
 __device__ __forceinline__ long long range_start(const KArgs& a, long long r) {
     return r * a.L / a.R;
 }
 
-// Index of the range that contains step s (inverse of range_start).
-__device__ __forceinline__ int range_of(const KArgs& a, long long s) {
-    return (int)(((s + 1) * (long long)a.R - 1) / a.L);
+// Index of the range that contains step q (inverse of range_start).
+__device__ __forceinline__ int range_of(const KArgs& a, long long q) {
+    return (int)(((q + 1) * (long long)a.R - 1) / a.L);
 }
 
+// Position in this CTA's step sequence: ranges blockIdx.x, +grid, +2*grid, ...
+struct StepCursor {
+    int r, q, q_end, rb, cb;  // range, step, range end, row block, step within row block
+    __device__ __forceinline__ void start_range(const KArgs& a) {
+        if (r < a.R) {
+            q = (int)range_start(a, r);
+            q_end = (int)range_start(a, r + 1);
+            rb = q / a.CS;
+            cb = q % a.CS;
+        }
+    }
+    __device__ __forceinline__ void init(const KArgs& a) {
+        r = blockIdx.x;
+        start_range(a);
+    }
+    __device__ __forceinline__ bool valid(const KArgs& a) const { return r < a.R; }
+    __device__ __forceinline__ void advance(const KArgs& a) {
+        if (r >= a.R) return;
+        ++q;
+        if (++cb == a.CS) {
+            cb = 0;
+            ++rb;
+        }
+        if (q == q_end) {
+            r += a.grid;
+            start_range(a);
+        }
+    }
+};
+
+// h = bf16(act(g) * u) for bf16-valued g, u.
 // SiLU(t) = t / (1 + e^-t).  GeLU (tanh form) 0.5 t (1 + tanh(z)) with
 // z = sqrt(2/pi) (t + 0.044715 t^3) is evaluated through the identity
-// 1 + tanh(z) = 2 / (1 + e^-2z), i.e. t / (1 + e^-2z): the same full-accuracy
-// expf as SiLU and no cancellation in 1 + tanh(z) for negative t.
-__device__ __forceinline__ float act_fn(int act, float t) {
-    if (act == 0) return t / (1.0f + expf(-t));
-    const float two_c = 1.5957691216057308f;  // 2 * sqrt(2/pi)
-    return t / (1.0f + expf(-two_c * (t + 0.044715f * t * t * t)));
+// 1 + tanh(z) = 2 / (1 + e^-2z), i.e. t / (1 + e^-2z): the same expf as SiLU
+// and no cancellation in 1 + tanh(z) for negative t.
+// When 1 + e rounds to exactly 1 in fp32, act(g) = g to fp32 precision while
+// the exact act(g) is slightly smaller in magnitude; g*u is then exact in fp32,
+// and an exact bf16 tie of it must round toward zero, as the exact product
+// (strictly inside the tie) does.
+__device__ __forceinline__ __nv_bfloat16 gated_product(int act, float g, float u) {
+    const float z = (act == 0) ? g : 1.5957691216057308f * (g + 0.044715f * g * g * g);
+    const float den = 1.0f + expf(-z);
+    const float p = (g / den) * u;
+    if (den == 1.0f) {
+        const uint32_t bits = __float_as_uint(p);
+        if ((bits & 0xFFFFu) == 0x8000u) return __ushort_as_bfloat16((unsigned short)(bits >> 16));
+    }
+    return __float2bfloat16_rn(p);
 }
 
 template <int NS>
@@ -142,43 +193,68 @@ __device__ __forceinline__ void store_output(const KArgs& a, int row, int token,
     } else {
         const float gb = __bfloat162float(__float2bfloat16_rn(va * a.scale_a));
         const float ub = __bfloat162float(__float2bfloat16_rn(vb * a.scale_b));
-        a.out[(size_t)token * a.N + row] = __float2bfloat16_rn(act_fn(a.act, gb) * ub);
+        a.out[(size_t)token * a.N + row] = gated_product(a.act, gb, ub);
     }
 }
 
+// Error-free addition (Knuth's TwoSum): hi + lo gains b exactly.
+__device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float b) {
+    const float s = hi + b;
+    const float bb = s - hi;
+    const float err = (hi - (s - bb)) + (b - bb);
+    hi = s;
+    lo += err;
+}
+
 // Stage the token rows for chunks c_start .. c_start+nx-1 (mod C) into shared
-// memory as f16 B fragments, after scaling token m by tok_scale[m] = 2^e_m.
+// memory as f16, token-major, in the order the B fragments are read: for token
+// m and chunk ci, 128 bytes at m*x_stride + ci*128, where lane quarter t owns
+// 32 bytes = the k pairs (16j+2t, +1) and (16j+2t+8, +9) of blocks j = 0..3.
+// One coalesced global pass (16-byte loads) scatters the bf16 values into
+// place and tracks each token's amax; a second, shared-memory-only pass scales
+// token m by 2^e_m (amax * 2^e_m in [2^14, 2^15)) and rounds to f16, which is
+// exact for every bf16 value within 2^-24 of the row's amax.
 template <int NT>
-__device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float* tok_scale,
-                        float* tok_unscale, unsigned* amax_u) {
-    const int ctid = threadIdx.x, lane = ctid & 31;
-    if (ctid < 16) amax_u[ctid] = 0u;
-    named_barrier_sync(kConsumerBarrier, kConsumerThreads);
-    const int groups = nx * 8;  // groups of 8 consecutive K elements
-    for (int m = 0; m < a.M; ++m) {
-        const __nv_bfloat16* xr = a.x + (size_t)m * a.K;
+__device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float* tok_unscale,
+                        unsigned* amax_u) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (tid < 16) amax_u[tid] = 0u;
+    __syncthreads();
+    const int per_token = nx * 8;  // 16-byte groups of 8 k per token
+    const int items = a.M * per_token;
+    float mx_local = 0.0f;
+    int m_local = -1;
+    for (int it = tid; it < items; it += kThreads) {
+        const int m = it / per_token, q = it - m * per_token;
+        const int ci = q >> 3, grp = q & 7;  // grp: k0 = 8*grp within the chunk
+        int c = c_start + ci;
+        if (c >= a.C) c -= a.C;
+        const int k0 = c * kChunkK + grp * 8;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (k0 < a.K) v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)m * a.K + k0));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         float mx = 0.0f;
-        for (int q = ctid; q < groups; q += kConsumerThreads) {
-            int c = c_start + (q >> 3);
-            if (c >= a.C) c -= a.C;
-            const int k = c * kChunkK + (q & 7) * 8;
-            if (k < a.K) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + k));
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    mx = fmaxf(mx, fabsf(__uint_as_float(w[i] << 16)));
-                    mx = fmaxf(mx, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
-                }
-            }
+        for (int i = 0; i < 4; ++i) {
+            mx = fmaxf(mx, fabsf(__uint_as_float(w[i] << 16)));
+            mx = fmaxf(mx, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
         }
+        // pair i (k = k0 + 2i, +1) belongs to lane quarter t = i, block j = grp/2,
+        // half = grp&1 (b0 for k%16 < 8, b1 otherwise)
+        uint8_t* base = xs + m * a.x_stride + ci * 128 + (grp >> 1) * 8 + (grp & 1) * 4;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (lane == 0 && mx > 0.0f) atomicMax(&amax_u[m], __float_as_uint(mx));
+        for (int i = 0; i < 4; ++i) *reinterpret_cast<uint32_t*>(base + i * 32) = w[i];
+        if (m != m_local) {
+            if (m_local >= 0 && mx_local > 0.0f) atomicMax(&amax_u[m_local], __float_as_uint(mx_local));
+            m_local = m;
+            mx_local = 0.0f;
+        }
+        mx_local = fmaxf(mx_local, mx);
     }
-    named_barrier_sync(kConsumerBarrier, kConsumerThreads);
-    if (ctid < 16) {
-        const float am = __uint_as_float(amax_u[ctid]);
+    if (m_local >= 0 && mx_local > 0.0f) atomicMax(&amax_u[m_local], __float_as_uint(mx_local));
+    __syncthreads();
+    if (tid < 16) {
+        const float am = __uint_as_float(amax_u[tid]);
         int e = 0;
         if (am > 0.0f) {
             int ex;
@@ -186,284 +262,351 @@ __device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float*
             e = 15 - ex;
             e = e < -100 ? -100 : (e > 100 ? 100 : e);
         }
-        tok_scale[ctid] = __int_as_float((127 + e) << 23);
-        tok_unscale[ctid] = __int_as_float((127 - e) << 23);
+        amax_u[tid] = (unsigned)(e + 128);  // reuse: biased exponent for the second pass
+        tok_unscale[tid] = __int_as_float((127 - e) << 23);
     }
-    named_barrier_sync(kConsumerBarrier, kConsumerThreads);
-    const int items = nx * NT * 64;
-    for (int it = ctid; it < items; it += kConsumerThreads) {
-        const int ln = it & 31, h = (it >> 5) & 1, q = it >> 6;
-        const int nt = q % NT, ci = q / NT;
-        int c = c_start + ci;
-        if (c >= a.C) c -= a.C;
-        const int token = nt * 8 + (ln >> 2), tq = ln & 3;
-        uint32_t o[4] = {0u, 0u, 0u, 0u};
-        if (token < a.M) {
-            const float sc = tok_scale[token];
-            const __nv_bfloat16* xr = a.x + (size_t)token * a.K;
+    __syncthreads();
+    const int words = a.M * nx * 32;  // 32-bit words (bf16 pairs) to convert
+    for (int it = tid; it < words; it += kThreads) {
+        const int m = it / (nx * 32), wi = it - m * (nx * 32);
+        uint32_t* p = reinterpret_cast<uint32_t*>(xs + m * a.x_stride) + wi;
+        const float sc = __int_as_float(((int)amax_u[m] - 128 + 127) << 23);
+        const uint32_t pr = *p;
+        const __half2 hv = __floats2half2_rn(__uint_as_float(pr << 16) * sc,
+                                             __uint_as_float(pr & 0xFFFF0000u) * sc);
+        *p = *reinterpret_cast<const uint32_t*>(&hv);
+    }
+    (void)lane;
+    __syncthreads();
+}
+
+// Split-K bookkeeping of one warp's tile.  Slot (range r, segment index) holds,
+// per tile, that range's fp32 partial sums of the tile's 16 rows x TOK tokens
+// for each stream; a per-(row block, tile) counter names the last range to
+// arrive, which sums all parts in range order.
+template <int NS, int NT>
+__device__ __forceinline__ float* tile_slot(const KArgs& a, int r, int rb, int warp) {
+    constexpr int TOK = NT * 8;
+    constexpr int SLOT = kBlockTiles * NS * kTileRows * TOK;
+    const int si_slot = rb - (int)(range_start(a, r) / a.CS);
+    return a.partials + ((size_t)r * a.s_max + si_slot) * SLOT + (size_t)warp * NS * kTileRows * TOK;
+}
+
+// End of the segment of row block rb (last step cb_last) that range r covers,
+// for this warp's tile; no CTA-wide synchronisation.  A segment spanning the
+// whole K range is stored at once.  Otherwise the partial goes to the range's
+// slot; returns true when this warp arrived last for its tile and must reduce
+// it (done later, off the streaming path, by reduce_tile).
+template <int NS, int NT>
+__device__ __forceinline__ bool finish_segment(const KArgs& a, float (&hi)[NS][NT][4],
+                                               float (&lo)[NS][NT][4],
+                                               const float (&unscale)[NT][2], int r, int q0,
+                                               int rb, int cb_last, int warp, int lane, bool ok) {
+    constexpr int TOK = NT * 8;
+    const int g = lane >> 2, tq = lane & 3;
+    const int seg_lo = q0 > rb * a.CS ? q0 : rb * a.CS;
+    const bool full_cover = (seg_lo == rb * a.CS) && (cb_last == a.CS - 1);
+    float v[NS][NT][4];
 #pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
+    for (int si = 0; si < NS; ++si)
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int k = c * kChunkK + 16 * (2 * h + jj) + 2 * tq + 8 * hf;
-                    if (k < a.K) {
-                        const uint32_t pr = __ldg(reinterpret_cast<const unsigned*>(xr + k));
-                        const __half2 hv = __floats2half2_rn(__uint_as_float(pr << 16) * sc,
-                                                             __uint_as_float(pr & 0xFFFF0000u) * sc);
-                        o[2 * jj + hf] = *reinterpret_cast<const uint32_t*>(&hv);
-                    }
-                }
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                v[si][nt][e] = (hi[si][nt][e] + lo[si][nt][e]) * unscale[nt][e & 1];
+                hi[si][nt][e] = 0.0f;
+                lo[si][nt][e] = 0.0f;
+            }
+    if (full_cover) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int row = rb * kBlockRows + warp * kTileRows + g + 8 * (e >> 1);
+                const int token = nt * 8 + 2 * tq + (e & 1);
+                if (ok && row < a.N && token < a.M)
+                    store_output<NS>(a, row, token, v[0][nt][e], v[NS - 1][nt][e]);
+            }
+        return false;
+    }
+    float* slot = tile_slot<NS, NT>(a, r, rb, warp);
+#pragma unroll
+    for (int si = 0; si < NS; ++si)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                slot[(si * kTileRows + g + 8 * (e >> 1)) * TOK + nt * 8 + 2 * tq + (e & 1)] =
+                    v[si][nt][e];
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+        const long long p_lo = (long long)rb * a.CS;
+        const int nparts = range_of(a, p_lo + a.CS - 1) - range_of(a, p_lo) + 1;
+        int* cnt = a.counters + rb * kBlockTiles + warp;
+        const int old = atomicAdd(cnt, 1);
+        last = (old == nparts - 1) ? 1 : 0;
+        if (last) {
+            *cnt = 0;  // ready for the next call
+            __threadfence();
+        }
+    }
+    return __shfl_sync(0xffffffffu, last, 0) != 0;
+}
+
+// The last range to arrive for (row block rb, this warp's tile): sum every
+// range's partial in range order and store the tile's outputs.
+template <int NS, int NT>
+__device__ __forceinline__ void reduce_tile(const KArgs& a, int rb, int warp, int lane, bool ok) {
+    constexpr int TOK = NT * 8;
+    const long long p_lo = (long long)rb * a.CS;
+    const int r_first = range_of(a, p_lo), r_last = range_of(a, p_lo + a.CS - 1);
+    for (int e = lane; e < kTileRows * a.M; e += 32) {
+        const int token = e % a.M, row16 = e / a.M;
+        const int row = rb * kBlockRows + warp * kTileRows + row16;
+        if (row >= a.N) continue;
+        float sum[NS];
+#pragma unroll
+        for (int si = 0; si < NS; ++si) sum[si] = 0.0f;
+        for (int rr = r_first; rr <= r_last; ++rr) {
+            const float* sl = tile_slot<NS, NT>(a, rr, rb, warp);
+#pragma unroll
+            for (int si = 0; si < NS; ++si) sum[si] += __ldcg(sl + (si * kTileRows + row16) * TOK + token);
+        }
+        if (ok) store_output<NS>(a, row, token, sum[0], sum[NS - 1]);
+    }
+}
+
+// One chunk (64 K elements) of the current step for this warp.  Per k16
+// block: the E2M1 codes become exact f16 A fragments (one cvt per byte), the
+// MMA forms the block's dot products against the staged token fragments from
+// a zero accumulator, and the two row scales (E4M3 -> f16 -> f32, exact) are
+// applied to those fp32 block sums with FFMAs.  Every MMA is independent; the
+// FMA pipe takes the scaling, which leaves the ALU pipe to the decode.
+template <int NS, int NT>
+__device__ __forceinline__ void process_chunk(const uint8_t* stage, const uint8_t* xs,
+                                              int x_stride, int M, int j, int cj, int warp,
+                                              int lane, float (&acc)[NS][NT][4]) {
+    constexpr int UB = kUnitBytes * NS;
+    const int g = lane >> 2, tq = lane & 3;
+    uint32_t b[NT][8];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int token = nt * 8 + g;  // B column (token row of x) this lane supplies
+        uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+        if (token < M) {
+            const uint8_t* px = xs + token * x_stride + cj * 128 + tq * 32;
+            v0 = *reinterpret_cast<const uint4*>(px);
+            v1 = *reinterpret_cast<const uint4*>(px + 16);
+        }
+        b[nt][0] = v0.x;
+        b[nt][1] = v0.y;
+        b[nt][2] = v0.z;
+        b[nt][3] = v0.w;
+        b[nt][4] = v1.x;
+        b[nt][5] = v1.y;
+        b[nt][6] = v1.z;
+        b[nt][7] = v1.w;
+    }
+    const uint8_t* unit = stage + (j * kBlockTiles + warp) * UB;
+#pragma unroll
+    for (int si = 0; si < NS; ++si) {
+        const uint4 cw = *reinterpret_cast<const uint4*>(unit + si * kUnitBytes + lane * 16);
+        const uint2 sw =
+            *reinterpret_cast<const uint2*>(unit + si * kUnitBytes + kUnitCodeBytes + g * 8);
+        const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+        for (int jb = 0; jb < 4; ++jb) {
+            uint32_t a0, a1, a2, a3;
+            e2m1x8_to_f16x2x4(cws[jb], a0, a1, a2, a3);
+            const uint32_t sp = (jb & 1) ? ((jb < 2 ? sw.x : sw.y) >> 16) : (jb < 2 ? sw.x : sw.y);
+            const uint32_t s2 = e4m3x2_to_f16x2(sp);  // (row g, row g+8) scales
+            const float sg = __half2float(__ushort_as_half((unsigned short)(s2 & 0xFFFFu)));
+            const float sg8 = __half2float(__ushort_as_half((unsigned short)(s2 >> 16)));
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                mma_f16_16816(d, a0, a1, a2, a3, b[nt][2 * jb], b[nt][2 * jb + 1]);
+                acc[si][nt][0] = fmaf(d[0], sg, acc[si][nt][0]);
+                acc[si][nt][1] = fmaf(d[1], sg, acc[si][nt][1]);
+                acc[si][nt][2] = fmaf(d[2], sg8, acc[si][nt][2]);
+                acc[si][nt][3] = fmaf(d[3], sg8, acc[si][nt][3]);
             }
         }
-        *reinterpret_cast<uint4*>(xs + ((ci * NT + nt) * 2 + h) * 512 + ln * 16) =
-            make_uint4(o[0], o[1], o[2], o[3]);
     }
-    named_barrier_sync(kConsumerBarrier, kConsumerThreads);
+}
+
+// Issue the bulk copy of the step at `cur` into ring stage st (one thread).
+template <int NS>
+__device__ __forceinline__ void issue_step(const KArgs& a, const StepCursor& cur, int st,
+                                           uint32_t ring_s, uint32_t full0, int* issues) {
+    constexpr int UB = kUnitBytes * NS;
+    constexpr int CPS = kUnitsPerStep / NS;
+    const uint32_t bytes = (uint32_t)(CPS * kBlockTiles * UB);
+    mbar_arrive_expect_tx(full0 + 8u * st, bytes);
+    bulk_copy_g2s(ring_s + (uint32_t)(st * a.stage_bytes),
+                  a.blob + ((size_t)cur.rb * a.C + (size_t)cur.cb * CPS) * kBlockTiles * UB, bytes,
+                  full0 + 8u * st);
+    ++issues[st];
 }
 
 template <int NS, int NT>
 __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a) {
-    constexpr int G = (NT == 1) ? 1 : 2;
-    constexpr int UB = kUnitBytes * NS;
-    constexpr int TOK = NT * 8;
-    constexpr int SLOT = G * kBlockTiles * NS * kTileRows * TOK;
+    constexpr int CPS = kUnitsPerStep / NS;  // chunks per step
 
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t ring_s = smem_addr(smem);
     uint8_t* xs = smem + a.x_off;
     const uint32_t full0 = smem_addr(smem + a.bar_off);
-    const uint32_t empty0 = full0 + 8u * a.stages;
-    float* tok_scale = reinterpret_cast<float*>(smem + a.misc_off);
-    float* tok_unscale = tok_scale + 16;
+    int* done = reinterpret_cast<int*>(smem + a.cnt_off);  // warps finished with a stage
+    int* issues = done + a.stages;                          // copies issued into a stage
+    float* tok_unscale = reinterpret_cast<float*>(smem + a.misc_off);
     unsigned* amax_u = reinterpret_cast<unsigned*>(tok_unscale + 16);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(amax_u + 16);
-    volatile int* last_flag = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tq = lane & 3;
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
             mbar_init(full0 + 8u * s, 1);
-            mbar_init(empty0 + 8u * s, kConsumerWarps);
+            done[s] = 0;
+            issues[s] = 0;
         }
         *abort_flag = 0;
-        *last_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
-
-    if (warp == kConsumerWarps) {
-        // ---------------- producer: one lane issues every bulk copy ----------------
-        if (lane != 0) return;
-        long long i = 0;
-        bool ok = true;
-        for (int r = blockIdx.x; r < a.R; r += a.grid) {
-            const long long s0 = range_start(a, r), s1 = range_start(a, r + 1);
-            for (long long s = s0; s < s1; ++s, ++i) {
-                const int st = (int)(i % a.stages);
-                const uint32_t ph = (uint32_t)((i / a.stages) & 1);
-                if (ok && !mbar_wait_bounded(empty0 + 8u * st, ph ^ 1u, abort_flag)) {
-                    ok = false;
-                    *abort_flag = 1;
-                    atomicOr(a.status, 1);
-                }
-                if (!ok) continue;
-                const int srb = (int)(s / a.C), c = (int)(s % a.C);
-                const int rb0 = srb * G;
-                const int np = (a.RB - rb0) < G ? (a.RB - rb0) : G;
-                mbar_arrive_expect_tx(full0 + 8u * st, (uint32_t)(np * kBlockTiles * UB));
-                for (int gi = 0; gi < np; ++gi) {
-                    bulk_copy_g2s(ring_s + (uint32_t)(st * a.stage_bytes + gi * kBlockTiles * UB),
-                                  a.blob + ((size_t)(rb0 + gi) * a.C + c) * kBlockTiles * UB,
-                                  (uint32_t)(kBlockTiles * UB), full0 + 8u * st);
-                }
+    // Let the next kernel on the stream launch as SMs free up; it will wait
+    // for this grid before it touches anything this grid writes.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Weights are never written by the preceding kernel when early_weights is
+    // set (the down projection after the dual kernel), so the ring can start
+    // filling before the wait; otherwise the wait comes first.
+    if (!a.early_weights) asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Initial fill of the ring; afterwards `ahead` (kept by every warp) points
+    // at the step one full ring ahead of the step being consumed.  Without
+    // early_weights the fill waits until the first range's token rows are in
+    // shared memory, so those few loads are not queued behind the burst.
+    StepCursor cur, ahead;
+    cur.init(a);
+    ahead.init(a);
+    bool filled = false;
+    auto fill_ring = [&]() {
+        if (threadIdx.x == 0) {
+            for (int st = 0; st < a.stages && ahead.valid(a); ++st) {
+                issue_step<NS>(a, ahead, st, ring_s, full0, issues);
+                ahead.advance(a);
             }
+        } else {
+            for (int st = 0; st < a.stages && ahead.valid(a); ++st) ahead.advance(a);
         }
-        // Drain: wait (bounded) until every copy issued by this CTA has landed.
-        const int zero = 0;
-        const long long first = i > a.stages ? i - a.stages : 0;
-        for (long long j = first; j < i; ++j)
-            mbar_wait_bounded(full0 + 8u * (int)(j % a.stages), (uint32_t)((j / a.stages) & 1),
-                              &zero);
-        return;
+        filled = true;
+    };
+    if (a.early_weights) {
+        fill_ring();
+        asm volatile("griddepcontrol.wait;" ::: "memory");
     }
 
-    // ---------------- consumers ----------------
-    const int g = lane >> 2, tq = lane & 3;
-    float acc[G][NS][NT][2][4];
+    float acc[NS][NT][4], hi[NS][NT][4], lo[NS][NT][4];
 #pragma unroll
-    for (int gi = 0; gi < G; ++gi)
+    for (int si = 0; si < NS; ++si)
 #pragma unroll
-        for (int si = 0; si < NS; ++si)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int ch = 0; ch < 2; ++ch)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[gi][si][nt][ch][e] = 0.0f;
-
-    long long i = 0;
+            for (int e = 0; e < 4; ++e) {
+                acc[si][nt][e] = 0.0f;
+                hi[si][nt][e] = 0.0f;
+                lo[si][nt][e] = 0.0f;
+            }
+    int st = 0;
+    uint32_t ph = 0;
     bool ok = true;
-    for (int r = blockIdx.x; r < a.R; r += a.grid) {
-        const long long s0 = range_start(a, r), s1 = range_start(a, r + 1);
-        const int c_start = (int)(s0 % a.C);
-        const int nx = (int)((s1 - s0) < a.C ? (s1 - s0) : a.C);
-        named_barrier_sync(kConsumerBarrier, kConsumerThreads);  // x buffer is free
-        stage_x<NT>(a, xs, c_start, nx, tok_scale, tok_unscale, amax_u);
+    // row blocks whose tile this warp must still reduce (arrived last)
+    constexpr int kMaxDeferred = 4;
+    int deferred[kMaxDeferred];
+    int n_deferred = 0;
+    while (cur.valid(a)) {
+        // ---- a new range: stage its token rows
+        const int r = cur.r, q0 = cur.q, q1 = cur.q_end;
+        const int c_start = cur.cb * CPS;
+        const int nx = (q1 - q0) * CPS < a.C ? (q1 - q0) * CPS : a.C;
+        __syncthreads();  // every warp is done with the previous range's x
+        stage_x<NT>(a, xs, c_start, nx, tok_unscale, amax_u);
+        if (!filled) fill_ring();
         float unscale[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) unscale[nt][e] = tok_unscale[nt * 8 + 2 * tq + e];
-
-        for (long long s = s0; s < s1; ++s, ++i) {
-            const int st = (int)(i % a.stages);
-            const uint32_t ph = (uint32_t)((i / a.stages) & 1);
+        int ci = 0, folded = 0;
+        while (cur.valid(a) && cur.r == r) {
             if (ok && !mbar_wait_bounded(full0 + 8u * st, ph, abort_flag)) {
                 ok = false;
                 *abort_flag = 1;
                 atomicOr(a.status, 1);
             }
-            const int srb = (int)(s / a.C), c = (int)(s % a.C);
             if (ok) {
-                int ci = c - c_start;
-                if (ci < 0) ci += a.C;
-                uint32_t b[NT][8];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint4 v = *reinterpret_cast<const uint4*>(
-                            xs + ((ci * NT + nt) * 2 + h) * 512 + lane * 16);
-                        b[nt][4 * h + 0] = v.x;
-                        b[nt][4 * h + 1] = v.y;
-                        b[nt][4 * h + 2] = v.z;
-                        b[nt][4 * h + 3] = v.w;
-                    }
                 const uint8_t* stage = smem + (size_t)st * a.stage_bytes;
 #pragma unroll
-                for (int gi = 0; gi < G; ++gi) {
-                    if (G > 1 && srb * G + gi >= a.RB) continue;
-                    const uint8_t* unit = stage + (gi * kBlockTiles + warp) * UB;
-#pragma unroll
-                    for (int si = 0; si < NS; ++si) {
-                        const uint4 cw =
-                            *reinterpret_cast<const uint4*>(unit + si * kUnitBytes + lane * 16);
-                        const uint2 sw = *reinterpret_cast<const uint2*>(
-                            unit + si * kUnitBytes + kUnitCodeBytes + g * 8);
-                        const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            uint32_t a0, a1, a2, a3;
-                            e2m1x8_to_f16x2x4(cws[j], a0, a1, a2, a3);
-                            const uint32_t sp = ((j < 2 ? sw.x : sw.y) >> (16 * (j & 1))) & 0xFFFFu;
-                            const uint32_t s2 = e4m3x2_to_f16x2(sp);
-                            const uint32_t sg = prmt(s2, s2, 0x1010u);
-                            const uint32_t sg8 = prmt(s2, s2, 0x3232u);
-                            a0 = hmul2(a0, sg);
-                            a2 = hmul2(a2, sg);
-                            a1 = hmul2(a1, sg8);
-                            a3 = hmul2(a3, sg8);
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt)
-                                mma_f16_16816(acc[gi][si][nt][j & 1], a0, a1, a2, a3,
-                                              b[nt][2 * j], b[nt][2 * j + 1]);
-                        }
-                    }
-                }
+                for (int j = 0; j < CPS; ++j)
+                    process_chunk<NS, NT>(stage, xs, a.x_stride, a.M, j, ci + j, warp, lane, acc);
             }
+            // Release the stage; the last warp out refills it a ring ahead.
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8u * st);
-
-            if (c != a.C - 1 && s != s1 - 1) continue;
-            // ---------------- end of a segment of row block srb ----------------
-            const long long seg_lo = s0 > (long long)srb * a.C ? s0 : (long long)srb * a.C;
-            const bool full_cover = (seg_lo == (long long)srb * a.C) && (c == a.C - 1);
-            float v[G][NS][NT][4];
-#pragma unroll
-            for (int gi = 0; gi < G; ++gi)
-#pragma unroll
-                for (int si = 0; si < NS; ++si)
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            v[gi][si][nt][e] = (acc[gi][si][nt][0][e] + acc[gi][si][nt][1][e]) *
-                                               unscale[nt][e & 1];
-                            acc[gi][si][nt][0][e] = 0.0f;
-                            acc[gi][si][nt][1][e] = 0.0f;
-                        }
-            if (full_cover) {
-#pragma unroll
-                for (int gi = 0; gi < G; ++gi)
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int row = (srb * G + gi) * kBlockRows + warp * kTileRows + g +
-                                            8 * (e >> 1);
-                            const int token = nt * 8 + 2 * tq + (e & 1);
-                            if (ok && row < a.N && token < a.M)
-                                store_output<NS>(a, row, token, v[gi][0][nt][e],
-                                                 v[gi][NS - 1][nt][e]);
-                        }
-                continue;
-            }
-            // Partial: write this range's slot, then let the last range finish.
-            const int si_slot = srb - (int)(s0 / a.C);
-            float* slot = a.partials + ((size_t)r * a.s_max + si_slot) * SLOT;
-#pragma unroll
-            for (int gi = 0; gi < G; ++gi)
-#pragma unroll
-                for (int si = 0; si < NS; ++si)
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int idx =
-                                (((gi * kBlockTiles + warp) * NS + si) * kTileRows + g + 8 * (e >> 1)) *
-                                    TOK +
-                                nt * 8 + 2 * tq + (e & 1);
-                            slot[idx] = v[gi][si][nt][e];
-                        }
-            __threadfence();
-            named_barrier_sync(kConsumerBarrier, kConsumerThreads);
-            const long long p_lo = (long long)srb * a.C;
-            const int r_first = range_of(a, p_lo), r_last = range_of(a, p_lo + a.C - 1);
-            if (threadIdx.x == 0) {
-                const int nparts = r_last - r_first + 1;
-                const int old = atomicAdd(&a.counters[srb], 1);
-                const int last = (old == nparts - 1) ? 1 : 0;
-                if (last) {
-                    a.counters[srb] = 0;  // ready for the next call
-                    __threadfence();
-                }
-                *last_flag = last;
-            }
-            named_barrier_sync(kConsumerBarrier, kConsumerThreads);
-            if (*last_flag) {
-                const int elems = G * kBlockTiles * kTileRows * a.M;
-                for (int e = threadIdx.x; e < elems; e += kConsumerThreads) {
-                    const int token = e % a.M;
-                    const int rest = e / a.M;
-                    const int row16 = rest % kTileRows;
-                    const int tis = rest / kTileRows;  // tile within the super row block
-                    const int row = srb * G * kBlockRows + tis * kTileRows + row16;
-                    if (row >= a.N) continue;
-                    float sum[NS];
-#pragma unroll
-                    for (int si = 0; si < NS; ++si) sum[si] = 0.0f;
-                    for (int rr = r_first; rr <= r_last; ++rr) {
-                        const int ss = srb - (int)(range_start(a, rr) / a.C);
-                        const float* sl = a.partials + ((size_t)rr * a.s_max + ss) * SLOT;
-#pragma unroll
-                        for (int si = 0; si < NS; ++si)
-                            sum[si] += __ldcg(sl + ((tis * NS + si) * kTileRows + row16) * TOK + token);
+            if (lane == 0) {
+                __threadfence_block();
+                const int old = atomicAdd(&done[st], 1);
+                if (old == kWarps - 1) {
+                    done[st] = 0;
+                    __threadfence_block();
+                    if (ahead.valid(a) && !*abort_flag) {
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        issue_step<NS>(a, ahead, st, ring_s, full0, issues);
                     }
-                    if (ok) store_output<NS>(a, row, token, sum[0], sum[NS - 1]);
                 }
             }
-            named_barrier_sync(kConsumerBarrier, kConsumerThreads);
+            ahead.advance(a);
+            if (++st == a.stages) {
+                st = 0;
+                ph ^= 1u;
+            }
+            const int rb_now = cur.rb, cb_now = cur.cb;
+            cur.advance(a);
+            ci += CPS;
+            if (ci >= a.C) ci -= a.C;
+            folded += CPS;
+            const bool seg_end = (cb_now == a.CS - 1) || (cur.r != r) || !cur.valid(a);
+            if (folded >= kFoldChunks || seg_end) {
+                folded = 0;
+#pragma unroll
+                for (int si = 0; si < NS; ++si)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            two_sum_acc(hi[si][nt][e], lo[si][nt][e], acc[si][nt][e]);
+                            acc[si][nt][e] = 0.0f;
+                        }
+            }
+            if (seg_end &&
+                finish_segment<NS, NT>(a, hi, lo, unscale, r, q0, rb_now, cb_now, warp, lane, ok)) {
+                if (n_deferred < kMaxDeferred)
+                    deferred[n_deferred++] = rb_now;
+                else
+                    reduce_tile<NS, NT>(a, rb_now, warp, lane, ok);
+            }
         }
+    }
+    for (int i = 0; i < n_deferred; ++i) reduce_tile<NS, NT>(a, deferred[i], warp, lane, ok);
+    // A CTA that abandoned a wait still owns copies in flight: wait for them
+    // (bounded) before the shared memory is released.
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) {
+        const int zero = 0;
+        for (int s = 0; s < a.stages; ++s)
+            if (issues[s] > 0)
+                mbar_wait_bounded(full0 + 8u * s, (uint32_t)((issues[s] - 1) & 1), &zero);
     }
 }
 
@@ -500,13 +643,25 @@ static cudaError_t launch_t(const Plan& p, const KArgs& a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    stream_gemv_kernel<NS, NT><<<p.grid, kThreads, p.smem, s>>>(a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, stream_gemv_kernel<NS, NT>, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 cudaError_t launch_stream_gemv(int streams, const void* x, int M, int K, const void* packed, int N,
                                float scale_a, float scale_b, int act, void* out, int* status,
-                               void* scratch, size_t scratch_bytes, int num_sms, cudaStream_t s) {
+                               void* scratch, size_t scratch_bytes, int num_sms, bool early_weights,
+                               cudaStream_t s) {
     const Plan p = make_plan(streams, M, N, K, num_sms);
     if (scratch_bytes < p.total) return cudaErrorInvalidValue;
     KArgs a;
@@ -521,18 +676,22 @@ cudaError_t launch_stream_gemv(int streams, const void* x, int M, int K, const v
     a.K = K;
     a.N = N;
     a.C = p.C;
+    a.CS = p.CS;
     a.RB = p.RB;
     a.R = p.R;
     a.grid = p.grid;
     a.stages = p.stages;
     a.stage_bytes = p.stage_bytes;
     a.x_off = p.x_off;
+    a.x_stride = p.x_stride;
     a.bar_off = p.bar_off;
+    a.cnt_off = p.cnt_off;
     a.misc_off = p.misc_off;
     a.s_max = p.s_max;
     a.scale_a = scale_a;
     a.scale_b = scale_b;
     a.act = act;
+    a.early_weights = early_weights ? 1 : 0;
     if (streams == 1)
         return p.NT == 1 ? launch_t<1, 1>(p, a, s) : launch_t<1, 2>(p, a, s);
     return p.NT == 1 ? launch_t<2, 1>(p, a, s) : launch_t<2, 2>(p, a, s);

@@ -41,11 +41,12 @@ def test_status_strings(lib):
 
 def test_repacked_sizes(lib):
     # aligned shapes keep the canonical byte count N*K*9/16
-    for N, K in ((5120, 17408), (17408, 5120), (4096, 4096), (128, 64)):
+    for N, K in ((5120, 17408), (17408, 5120), (4096, 4096), (256, 256), (21504, 5376)):
         assert lib.nvfp4_repacked_bytes(N, K) == N * K * 9 // 16
         assert lib.nvfp4_repacked_gate_up_bytes(N, K) == 2 * N * K * 9 // 16
-    # ragged shapes are zero-padded to 128 rows x 64 columns
-    assert lib.nvfp4_repacked_bytes(200, 272) == 256 * 320 * 9 // 16
+    # ragged shapes are zero-padded to 256 rows x 256 columns
+    assert lib.nvfp4_repacked_bytes(200, 272) == 256 * 512 * 9 // 16
+    assert lib.nvfp4_repacked_bytes(300, 16) == 512 * 256 * 9 // 16
     assert lib.nvfp4_repacked_bytes(0, 64) == 0
 
 
