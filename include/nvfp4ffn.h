@@ -182,6 +182,29 @@ nvfp4_status ffn_gate_up_nvfp4(const void* x, int M, int H, int I, const void* g
                                float gate_scale2, float up_scale2, nvfp4_act act, void* h,
                                void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * ffn_swiglu_nvfp4 for callers that cannot allocate device memory where they
+ * run the FFN (a process that reserves the device's memory for its own pool at
+ * start-up and forbids later cudaMalloc, or code that must not risk the
+ * implicit device synchronisation of an allocation).  The pages have no
+ * counterpart of this call; it exists for such callers.
+ *   Same arguments and results as ffn_swiglu_nvfp4, without ws/ws_bytes: the
+ *   workspace is one library-owned device array of 24 MiB, held by every GPU
+ *   that loads the library until the process exits.  Shapes whose
+ *   ffn_swiglu_nvfp4_workspace_bytes exceeds 24 MiB are rejected with
+ *   NVFP4_ERR_WORKSPACE (M = 16 at H = 5376, I = 21504 needs about 21 MiB).
+ *   The first call on each device resolves the array's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   Each call zero-fills the part of the array it uses on `stream` and then
+ *   runs the two FFN kernels there; it allocates nothing.  Every call shares
+ *   the one array, so calls that overlap on the GPU (different streams without
+ *   ordering between them) race and corrupt each other's results.
+ */
+nvfp4_status ffn_swiglu_nvfp4_noalloc(const void* x, int M, int H, int I,
+                                      const void* gate_up_packed, float gate_scale2,
+                                      float up_scale2, const void* down_packed, float down_scale2,
+                                      nvfp4_act act, void* out, cudaStream_t stream);
+
 /* ------------------------------------------------------------------ utilities */
 
 /* Zero-fill a workspace (asynchronous memset on `stream`). */

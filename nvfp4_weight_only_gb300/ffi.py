@@ -31,6 +31,7 @@ EXPORTS = [
     "nvfp4_repacked_gate_up_bytes", "nvfp4_repack_gate_up", "nvfp4_unpack",
     "nvfp4_gemv_workspace_bytes", "nvfp4_gemv", "ffn_swiglu_nvfp4_workspace_bytes",
     "ffn_swiglu_nvfp4", "ffn_gate_up_nvfp4_workspace_bytes", "ffn_gate_up_nvfp4",
+    "ffn_swiglu_nvfp4_noalloc",
     "nvfp4_workspace_init", "nvfp4_workspace_status", "nvfp4_status_string",
 ]
 
@@ -72,6 +73,7 @@ def load(build_if_missing: bool = False):
         "ffn_swiglu_nvfp4": (i32, [vp, i32, i32, i32, vp, f32, f32, vp, f32, i32, vp, vp, sz, vp]),
         "ffn_gate_up_nvfp4_workspace_bytes": (sz, [i32, i32, i32]),
         "ffn_gate_up_nvfp4": (i32, [vp, i32, i32, i32, vp, f32, f32, i32, vp, vp, sz, vp]),
+        "ffn_swiglu_nvfp4_noalloc": (i32, [vp, i32, i32, i32, vp, f32, f32, vp, f32, i32, vp, vp]),
         "nvfp4_workspace_init": (i32, [vp, sz, vp]),
         "nvfp4_workspace_status": (i32, [vp, vp]),
         "nvfp4_status_string": (ctypes.c_char_p, [i32]),
@@ -211,6 +213,28 @@ def ffn_swiglu_nvfp4(x: torch.Tensor, gate_up_packed: torch.Tensor, gate_scale2:
            L.ffn_swiglu_nvfp4(_ptr(x), M, H, I, _ptr(gate_up_packed), float(gate_scale2),
                               float(up_scale2), _ptr(down_packed), float(down_scale2), int(act),
                               _ptr(out), _ptr(ws), ws.numel(), _stream(x.device)))
+    return out
+
+
+def ffn_swiglu_nvfp4_noalloc(x: torch.Tensor, gate_up_packed: torch.Tensor, gate_scale2: float,
+                             up_scale2: float, down_packed: torch.Tensor, down_scale2: float,
+                             I: int, act: int = NVFP4_ACT_SILU,
+                             out: torch.Tensor = None) -> torch.Tensor:
+    """ffn_swiglu_nvfp4 on the library's fixed device workspace (for callers that
+    cannot allocate one); only the output is allocated here, and only when `out`
+    is not given."""
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(gate_up_packed, "gate_up_packed", torch.uint8)
+    _cuda(down_packed, "down_packed", torch.uint8)
+    M, H = x.shape
+    L = load()
+    if out is None:
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    _cuda(out, "out", torch.bfloat16)
+    _check("ffn_swiglu_nvfp4_noalloc",
+           L.ffn_swiglu_nvfp4_noalloc(_ptr(x), M, H, I, _ptr(gate_up_packed), float(gate_scale2),
+                                      float(up_scale2), _ptr(down_packed), float(down_scale2),
+                                      int(act), _ptr(out), _stream(x.device)))
     return out
 
 
