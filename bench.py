@@ -142,6 +142,23 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def reduce_max(values, device=None):
+    """Element-wise maximum of `values` over all ranks of the default process
+    group (identity on a single process)."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def whole_job_gbs(world, bytes_per_step, steps, seconds):
+    """Whole-job effective bandwidth: every rank's bytes over the slowest rank's time."""
+    return world * bytes_per_step * steps / seconds / 1e9
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -277,13 +294,9 @@ def run_ours(args, wl):
     if status != 0:
         raise RuntimeError(f"device status word reports {status} (bounded wait abandoned)")
 
-    t_max = t_step
-    if world > 1:
-        t = torch.tensor([t_step, t_e2e], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max, t_e2e = float(t[0]), float(t[1])
+    t_max, t_e2e = reduce_max([t_step, t_e2e], device=dev)
     per_step = layer_bytes(H, I, M) * L
-    value = world * per_step * args.steps / t_max / 1e9
+    value = whole_job_gbs(world, per_step, args.steps, t_max)
     us_layer = t_max / (args.steps * L) * 1e6
     peak, peak_kind = measured_peaks()
     dual_gbs = dual_kernel_bytes(H, I, M) / t_dual / 1e9
@@ -320,7 +333,7 @@ def run_ours(args, wl):
                             "unit": "GB/s", "frac": round(down_kernel_bytes(H, I, M) / t_down
                                                           / 1e9 / peak, 4),
                             "us_per_launch": round(t_down * 1e6, 3)},
-            "e2e": {"value": round(world * per_step / t_e2e / 1e9, 1), "unit": "GB/s",
+            "e2e": {"value": round(whole_job_gbs(world, per_step, 1, t_e2e), 1), "unit": "GB/s",
                     "h2d_bytes_per_step": M * H * 2, "d2h_bytes_per_step": M * H * 2,
                     "path": "per-layer ffn_swiglu_nvfp4 C-ABI calls, pinned host x/out"},
             "gpu_launches": 2 * L * args.steps,

@@ -58,6 +58,10 @@ def lib():
                               u8p, u8p, ctypes.c_float, u8p, u8p, ctypes.c_float,
                               ctypes.c_int, u16p]
         L.orc_ffn.restype = None
+        L.orc_bf16_from_double_array.argtypes = [f64p, i64, u16p]
+        L.orc_bf16_from_double_array.restype = None
+        L.orc_act_array.argtypes = [f64p, i64, ctypes.c_int, f64p]
+        L.orc_act_array.restype = None
         L.orc_set_threads.argtypes = [ctypes.c_int]
         L.orc_set_threads.restype = ctypes.c_int
         _lib = L
@@ -176,6 +180,22 @@ def ffn(x_bits, I, gate, up, down, act=ACT_SILU):
     lib().orc_ffn(x, M, H, I, _c(gate[0], np.uint8), _c(gate[1], np.uint8), gate[2],
                   _c(up[0], np.uint8), _c(up[1], np.uint8), up[2],
                   _c(down[0], np.uint8), _c(down[1], np.uint8), down[2], int(act), out)
+    return out
+
+
+def bf16_from_double_array(v):
+    """Elementwise bf16_from_double over a float64 array (same shape, uint16)."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.zeros(v.shape, np.uint16)
+    lib().orc_bf16_from_double_array(v.reshape(-1), v.size, out.reshape(-1))
+    return out
+
+
+def act_array(v, act=ACT_SILU):
+    """Elementwise SiLU (act=0) or GeLU-tanh (act=1) over a float64 array."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.zeros(v.shape, np.float64)
+    lib().orc_act_array(v.reshape(-1), v.size, int(act), out.reshape(-1))
     return out
 
 

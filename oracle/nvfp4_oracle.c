@@ -359,3 +359,18 @@ int orc_set_threads(int n)
     return 1;
 #endif
 }
+
+/* ---------------- array forms (loops over the functions above) ---------------- */
+
+void orc_bf16_from_double_array(const double *v, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_bf16_from_double(v[i]);
+}
+
+/* act: 0 = SiLU, 1 = GeLU (tanh) */
+void orc_act_array(const double *v, int64_t n, int act, double *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = (act == 0) ? orc_silu(v[i]) : orc_gelu_tanh(v[i]);
+}

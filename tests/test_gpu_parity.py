@@ -169,18 +169,77 @@ def build_ffn(dev, H, I, layer=0):
     return gu, dn, q, rq
 
 
+# A GPU accumulation order may legitimately round an intermediate either way
+# when its exact value lies within the accumulation error of a bf16 midpoint.
+# For a sum that error scales with sum_k |x_k w_k| (fp32, ~4e-7 of it with the
+# kernels' TwoSum folding), for a product with the product itself (~3e-7).
+FLIP_EPS = 2e-6
+
+
+def _bf16_pair(v, window):
+    """bf16 value nearest v, the other neighbour, and whether v lies within
+    `window` of their midpoint (where either rounding is correct)."""
+    r = oracle.bf16_bits_to_f64(oracle.bf16_from_double_array(v))
+    ulp = np.abs(r) * 2.0 ** -7 + 1e-300
+    lo = np.where(r <= v, r, r - ulp)
+    hi = np.where(r <= v, r + ulp, r)
+    near = np.abs(v - 0.5 * (lo + hi)) <= window
+    return r, np.where(r == lo, hi, lo), near
+
+
+def _abs_sum(x_bits, q, N):
+    """sum_k |x_k| |w_k| * scale2 of every output: the scale of its rounding error."""
+    codes = (q[0] & 0x77).astype(np.uint8)  # clear both nibbles' sign bits
+    return oracle.gemv_f64((x_bits & 0x7FFF).astype(np.uint16), codes, q[1], q[2], N)
+
+
+def check_hidden_valid(h_gpu_bits, x_bits, rq, act):
+    """Every GPU h element must be the oracle's h, or what the specified
+    roundings give when the exact g, u or act(g)*u lies within the accumulation
+    error of a bf16 midpoint (where either rounding is correct)."""
+    I = rq[0][0].shape[0]
+    g64 = oracle.gemv_f64(x_bits, rq[0][0], rq[0][1], rq[0][2], I)
+    u64 = oracle.gemv_f64(x_bits, rq[1][0], rq[1][1], rq[1][2], I)
+    h_gpu = oracle.bf16_bits_to_f64(h_gpu_bits)
+    gr, ga, gn = _bf16_pair(g64, FLIP_EPS * _abs_sum(x_bits, rq[0], I))
+    ur, ua, un = _bf16_pair(u64, FLIP_EPS * _abs_sum(x_bits, rq[1], I))
+    ok = np.zeros(h_gpu.shape, bool)
+    for gv, gmask in ((gr, None), (ga, gn)):
+        for uv, umask in ((ur, None), (ua, un)):
+            p = oracle.act_array(gv, act) * uv
+            pr, pa, pn = _bf16_pair(p, FLIP_EPS * np.abs(p))
+            allowed = np.ones(h_gpu.shape, bool)
+            if gmask is not None:
+                allowed &= gmask
+            if umask is not None:
+                allowed &= umask
+            ok |= allowed & ((h_gpu == pr) | (pn & (h_gpu == pa)))
+    bad = np.argwhere(~ok)
+    assert bad.size == 0, f"h: {len(bad)} elements not a valid rounding, first {bad[:5].tolist()}"
+
+
 def run_ffn_case(dev, H, I, M, act, outliers=0.0, seed=0, check_hidden=False):
+    """FFN parity.  The intermediate h is checked for validity (check_hidden_valid);
+    the output against the oracle's down projection of the GPU's own h (exact
+    tolerance); and end to end against the oracle, where elements may only
+    leave the tolerance through the legitimate h roundings (at most 0.5%)."""
     gu, dn, q, rq = build_ffn(dev, H, I)
     x = synth.activations_bf16(M, H, seed=seed, outlier_frac=outliers)
+    xb = synth.bf16_bits(x)
     ws = ffi.workspace(ffi.ffn_swiglu_nvfp4_workspace_bytes(M, H, I), dev)
     out = ffi.ffn_swiglu_nvfp4(x.to(dev), gu, q[0][2], q[1][2], dn, q[2][2], I, act, ws=ws)
-    ref = oracle.ffn(synth.bf16_bits(x), I, rq[0], rq[1], rq[2], act)
-    err = assert_close(out, ref, f"ffn H={H} I={I} M={M} act={act}")
-    if check_hidden:
-        h_ref = oracle.ffn_hidden(synth.bf16_bits(x), I, rq[0], rq[1], act)
-        assert_close(ffi.ffn_hidden_view(ws, M, I), h_ref, "ffn hidden h")
+    torch.cuda.synchronize()
+    h_bits = synth.bf16_bits(ffi.ffn_hidden_view(ws, M, I))
+    check_hidden_valid(h_bits, xb, rq, act)
+    err = assert_close(out, oracle.gemv(h_bits, rq[2][0], rq[2][1], rq[2][2], H),
+                       f"ffn down(h_gpu) H={H} I={I} M={M} act={act}")
+    ref = oracle.ffn(xb, I, rq[0], rq[1], rq[2], act)
+    g = out.float().cpu().double().numpy()
+    r = oracle.bf16_bits_to_f64(ref)
+    n_out = int(np.count_nonzero(np.abs(g - r) > TOL * np.maximum(1.0, np.abs(r))))
+    assert n_out <= 0.005 * r.size, f"ffn end to end: {n_out} of {r.size} out of tolerance"
     assert ffi.nvfp4_workspace_status(ws) == 0
-    return err
+    return err, n_out
 
 
 def test_ffn_tiny_config(dev):

@@ -393,3 +393,13 @@ def test_nibble_order_low_nibble_is_even_element():
     x[0, 3] = 0
     x[0, 2] = 0x3F80
     assert oracle.gemv_f64(x, codes, scales, s2, 1)[0, 0] == 0.0
+
+
+def test_array_forms_agree_with_scalar_functions():
+    rng = np.random.default_rng(21)
+    v = np.concatenate([rng.standard_normal(500) * 10.0 ** rng.integers(-5, 5, 500),
+                        [0.0, -0.0, 1 + 2 ** -8 + 2 ** -30]])
+    b = oracle.bf16_from_double_array(v)
+    assert [oracle.bf16_from_double(float(t)) for t in v] == list(b)
+    for act, fn in ((oracle.ACT_SILU, oracle.silu), (oracle.ACT_GELU_TANH, oracle.gelu_tanh)):
+        np.testing.assert_array_equal(oracle.act_array(v, act), [fn(float(t)) for t in v])
