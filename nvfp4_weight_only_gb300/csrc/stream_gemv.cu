@@ -104,7 +104,7 @@ static Plan make_plan(int NS, int M, int N, int K, int num_sms) {
     long long smax = ceil_div(p.Pmax, p.CS) + 1;
     if (smax > p.RB) smax = p.RB;
     p.s_max = (int)smax;
-    p.slot_floats = kBlockTiles * NS * kTileRows * (p.NT * 8);
+    p.slot_floats = kBlockTiles * NS * kTileRows * M;
     p.counters_off = 0;
     p.partials_off = (size_t)ceil_div((long long)p.RB * kBlockTiles * 4, 256) * 256;
     p.total = p.partials_off + (size_t)p.R * p.s_max * p.slot_floats * sizeof(float);
@@ -165,18 +165,22 @@ struct StepCursor {
     }
 };
 
-// h = bf16(act(g) * u) for bf16-valued g, u.
-// SiLU(t) = t / (1 + e^-t).  GeLU (tanh form) 0.5 t (1 + tanh(z)) with
-// z = sqrt(2/pi) (t + 0.044715 t^3) is evaluated through the identity
-// 1 + tanh(z) = 2 / (1 + e^-2z), i.e. t / (1 + e^-2z): the same expf as SiLU
-// and no cancellation in 1 + tanh(z) for negative t.
-// When 1 + e rounds to exactly 1 in fp32, act(g) = g to fp32 precision while
-// the exact act(g) is slightly smaller in magnitude; g*u is then exact in fp32,
-// and an exact bf16 tie of it must round toward zero, as the exact product
-// (strictly inside the tie) does.
+// h = bf16(act(g) * u) for bf16-valued g, u, with act(t) = t * sigmoid(y):
+// SiLU has y = t; GeLU (tanh form) 0.5 t (1 + tanh(z)) has y = 2z,
+// z = sqrt(2/pi) (t + 0.044715 t^3), by the identity 1 + tanh(z) = 2 sigmoid(2z).
+// sigmoid(y) is 1 / (1 + e^-y) for y >= 0 and e^y / (1 + e^y) for y < 0, so
+// neither branch overflows and the far negative tail keeps its (subnormal)
+// value instead of collapsing to zero.  When 1 + e^-y rounds to exactly 1 in
+// fp32, act(g) = g to fp32 precision while the exact act(g) is slightly
+// smaller in magnitude; g*u is then exact in fp32, and an exact bf16 tie of
+// it must round toward zero, as the exact product (strictly inside) does.
 __device__ __forceinline__ __nv_bfloat16 gated_product(int act, float g, float u) {
-    const float z = (act == 0) ? g : 1.5957691216057308f * (g + 0.044715f * g * g * g);
-    const float den = 1.0f + expf(-z);
+    const float y = (act == 0) ? g : 1.5957691216057308f * (g + 0.044715f * g * g * g);
+    if (y < 0.0f) {
+        const float e = expf(y);
+        return __float2bfloat16_rn(g * (e / (1.0f + e)) * u);
+    }
+    const float den = 1.0f + expf(-y);
     const float p = (g / den) * u;
     if (den == 1.0f) {
         const uint32_t bits = __float_as_uint(p);
@@ -284,25 +288,43 @@ __device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float*
 // per tile, that range's fp32 partial sums of the tile's 16 rows x TOK tokens
 // for each stream; a per-(row block, tile) counter names the last range to
 // arrive, which sums all parts in range order.
-template <int NS, int NT>
+template <int NS>
 __device__ __forceinline__ float* tile_slot(const KArgs& a, int r, int rb, int warp) {
-    constexpr int TOK = NT * 8;
-    constexpr int SLOT = kBlockTiles * NS * kTileRows * TOK;
+    const size_t slot = (size_t)kBlockTiles * NS * kTileRows * a.M;
     const int si_slot = rb - (int)(range_start(a, r) / a.CS);
-    return a.partials + ((size_t)r * a.s_max + si_slot) * SLOT + (size_t)warp * NS * kTileRows * TOK;
+    return a.partials + ((size_t)r * a.s_max + si_slot) * slot + (size_t)warp * NS * kTileRows * a.M;
+}
+
+// Count this warp's partial of (row block rb, tile) as arrived; true when it
+// was the last of the ranges covering rb, which then reduces the tile.  The
+// caller has fenced its slot stores (GPU scope) before calling.
+__device__ __forceinline__ bool publish_tile(const KArgs& a, int rb, int warp, int lane) {
+    int last = 0;
+    if (lane == 0) {
+        const long long p_lo = (long long)rb * a.CS;
+        const int nparts = range_of(a, p_lo + a.CS - 1) - range_of(a, p_lo) + 1;
+        int* cnt = a.counters + rb * kBlockTiles + warp;
+        const int old = atomicAdd(cnt, 1);
+        last = (old == nparts - 1) ? 1 : 0;
+        if (last) {
+            *cnt = 0;  // ready for the next call
+            __threadfence();
+        }
+    }
+    return __shfl_sync(0xffffffffu, last, 0) != 0;
 }
 
 // End of the segment of row block rb (last step cb_last) that range r covers,
 // for this warp's tile; no CTA-wide synchronisation.  A segment spanning the
-// whole K range is stored at once.  Otherwise the partial goes to the range's
-// slot; returns true when this warp arrived last for its tile and must reduce
-// it (done later, off the streaming path, by reduce_tile).
+// whole K range is stored at once.  Otherwise the fp32 partial goes to the
+// range's slot, is published (fence, then the tile's counter), and the
+// function returns true when this range arrived last for the tile and must
+// reduce it (done after the stream, by reduce_tile).
 template <int NS, int NT>
 __device__ __forceinline__ bool finish_segment(const KArgs& a, float (&hi)[NS][NT][4],
                                                float (&lo)[NS][NT][4],
                                                const float (&unscale)[NT][2], int r, int q0,
                                                int rb, int cb_last, int warp, int lane, bool ok) {
-    constexpr int TOK = NT * 8;
     const int g = lane >> 2, tq = lane & 3;
     const int seg_lo = q0 > rb * a.CS ? q0 : rb * a.CS;
     const bool full_cover = (seg_lo == rb * a.CS) && (cb_last == a.CS - 1);
@@ -329,37 +351,26 @@ __device__ __forceinline__ bool finish_segment(const KArgs& a, float (&hi)[NS][N
             }
         return false;
     }
-    float* slot = tile_slot<NS, NT>(a, r, rb, warp);
+    float* slot = tile_slot<NS>(a, r, rb, warp);
 #pragma unroll
     for (int si = 0; si < NS; ++si)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                slot[(si * kTileRows + g + 8 * (e >> 1)) * TOK + nt * 8 + 2 * tq + (e & 1)] =
-                    v[si][nt][e];
+            for (int e = 0; e < 4; ++e) {
+                const int token = nt * 8 + 2 * tq + (e & 1);
+                if (token < a.M)
+                    slot[(si * kTileRows + g + 8 * (e >> 1)) * a.M + token] = v[si][nt][e];
+            }
     __threadfence();
     __syncwarp();
-    int last = 0;
-    if (lane == 0) {
-        const long long p_lo = (long long)rb * a.CS;
-        const int nparts = range_of(a, p_lo + a.CS - 1) - range_of(a, p_lo) + 1;
-        int* cnt = a.counters + rb * kBlockTiles + warp;
-        const int old = atomicAdd(cnt, 1);
-        last = (old == nparts - 1) ? 1 : 0;
-        if (last) {
-            *cnt = 0;  // ready for the next call
-            __threadfence();
-        }
-    }
-    return __shfl_sync(0xffffffffu, last, 0) != 0;
+    return publish_tile(a, rb, warp, lane);
 }
 
 // The last range to arrive for (row block rb, this warp's tile): sum every
 // range's partial in range order and store the tile's outputs.
-template <int NS, int NT>
+template <int NS>
 __device__ __forceinline__ void reduce_tile(const KArgs& a, int rb, int warp, int lane, bool ok) {
-    constexpr int TOK = NT * 8;
     const long long p_lo = (long long)rb * a.CS;
     const int r_first = range_of(a, p_lo), r_last = range_of(a, p_lo + a.CS - 1);
     for (int e = lane; e < kTileRows * a.M; e += 32) {
@@ -370,9 +381,9 @@ __device__ __forceinline__ void reduce_tile(const KArgs& a, int rb, int warp, in
 #pragma unroll
         for (int si = 0; si < NS; ++si) sum[si] = 0.0f;
         for (int rr = r_first; rr <= r_last; ++rr) {
-            const float* sl = tile_slot<NS, NT>(a, rr, rb, warp);
+            const float* sl = tile_slot<NS>(a, rr, rb, warp);
 #pragma unroll
-            for (int si = 0; si < NS; ++si) sum[si] += __ldcg(sl + (si * kTileRows + row16) * TOK + token);
+            for (int si = 0; si < NS; ++si) sum[si] += __ldcg(sl + (si * kTileRows + row16) * a.M + token);
         }
         if (ok) store_output<NS>(a, row, token, sum[0], sum[NS - 1]);
     }
@@ -522,10 +533,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
     int st = 0;
     uint32_t ph = 0;
     bool ok = true;
-    // row blocks whose tile this warp must still reduce (arrived last)
-    constexpr int kMaxDeferred = 4;
-    int deferred[kMaxDeferred];
-    int n_deferred = 0;
+    // row blocks whose tile this warp must still reduce (it arrived last)
+    constexpr int kMaxPending = 4;
+    int pending[kMaxPending];
+    int n_pending = 0;
     while (cur.valid(a)) {
         // ---- a new range: stage its token rows
         const int r = cur.r, q0 = cur.q, q1 = cur.q_end;
@@ -591,14 +602,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
             }
             if (seg_end &&
                 finish_segment<NS, NT>(a, hi, lo, unscale, r, q0, rb_now, cb_now, warp, lane, ok)) {
-                if (n_deferred < kMaxDeferred)
-                    deferred[n_deferred++] = rb_now;
+                if (n_pending < kMaxPending)
+                    pending[n_pending++] = rb_now;
                 else
-                    reduce_tile<NS, NT>(a, rb_now, warp, lane, ok);
+                    reduce_tile<NS>(a, rb_now, warp, lane, ok);
             }
         }
     }
-    for (int i = 0; i < n_deferred; ++i) reduce_tile<NS, NT>(a, deferred[i], warp, lane, ok);
+    for (int i = 0; i < n_pending; ++i) reduce_tile<NS>(a, pending[i], warp, lane, ok);
     // A CTA that abandoned a wait still owns copies in flight: wait for them
     // (bounded) before the shared memory is released.
     __syncthreads();

@@ -162,6 +162,11 @@ def gelu_tanh(t: float) -> float:
     return lib().orc_gelu_tanh(t)
 
 
+def act(t: float, which: int = 0) -> float:
+    """SiLU (which=0) or GeLU-tanh (which=1) of one value."""
+    return silu(t) if which == ACT_SILU else gelu_tanh(t)
+
+
 def ffn_hidden(x_bits, I, gate, up, act=ACT_SILU):
     """gate/up = (codes, scales, scale2).  Returns h bf16 bits [M, I]."""
     x = _c(x_bits, np.uint16)

@@ -403,3 +403,21 @@ def test_array_forms_agree_with_scalar_functions():
     assert [oracle.bf16_from_double(float(t)) for t in v] == list(b)
     for act, fn in ((oracle.ACT_SILU, oracle.silu), (oracle.ACT_GELU_TANH, oracle.gelu_tanh)):
         np.testing.assert_array_equal(oracle.act_array(v, act), [fn(float(t)) for t in v])
+
+
+@pytest.mark.parametrize("t", [-12.0, -9.5, -7.0, -5.0, -3.0, -1.0, -0.01, 0.3, 2.0, 6.0, 11.0])
+def test_activations_match_high_precision_evaluation(t):
+    # Both activations in 150-digit decimal arithmetic straight from their
+    # definitions (tanh through exp); the oracle must agree to ~1e-14
+    # relative everywhere, including the far negative tails where a literal
+    # 1 + tanh(z) in double precision cancels.
+    from decimal import Decimal, getcontext
+    getcontext().prec = 150
+    T = Decimal(t)
+    pi = Decimal("3.14159265358979323846264338327950288419716939937510")
+    z = (Decimal(2) / pi).sqrt() * (T + Decimal("0.044715") * T ** 3)
+    tanh = ((2 * z).exp() - 1) / ((2 * z).exp() + 1)
+    gelu = Decimal("0.5") * T * (1 + tanh)
+    silu = T / (1 + (-T).exp())
+    assert oracle.gelu_tanh(t) == pytest.approx(float(gelu), rel=1e-14, abs=1e-300)
+    assert oracle.silu(t) == pytest.approx(float(silu), rel=1e-14, abs=1e-300)
