@@ -32,6 +32,13 @@
  *    through cudaGetLastError().
  *  - BF16 tensors are row-major with a row stride equal to their width.
  *  - Device pointers must be 16-byte aligned.
+ *  - The GEMV/FFN kernels use programmatic dependent launch: they may start
+ *    while the preceding kernel on `stream` is still finishing and begin
+ *    streaming their (repacked) weights at once; they read x and write every
+ *    output only after that kernel has completed.  So the weight buffers must
+ *    not be written by the kernel issued immediately before the call on the
+ *    same stream.  This library's quantise and repack calls are safe
+ *    predecessors (their blocks fence their stores before exiting).
  */
 #ifndef NVFP4FFN_H
 #define NVFP4FFN_H

@@ -137,7 +137,7 @@ nvfp4_status nvfp4_gemv(const void* x, int M, int K, const void* packed_w, float
     char* w = reinterpret_cast<char*>(ws);
     return cuda_status(nvf::launch_stream_gemv(1, x, M, K, packed_w, N, scale2, scale2, 0, y,
                                                reinterpret_cast<int*>(w), w + nvf::kStatusBytes,
-                                               need - nvf::kStatusBytes, sms, false, stream));
+                                               need - nvf::kStatusBytes, sms, true, stream));
 }
 
 size_t ffn_swiglu_nvfp4_workspace_bytes(int M, int H, int I) {
@@ -166,10 +166,8 @@ nvfp4_status ffn_swiglu_nvfp4(const void* x, int M, int H, int I, const void* ga
     void* h = w + l.h_off;
     cudaError_t e = nvf::launch_stream_gemv(2, x, M, H, gate_up_packed, I, gate_scale2, up_scale2,
                                             (int)act, h, status, w + l.dual_off, l.dual_bytes, sms,
-                                            false, stream);
+                                            true, stream);
     if (e != cudaSuccess) return NVFP4_ERR_CUDA;
-    // The down kernel follows the dual kernel, which never writes weights, so it
-    // may start streaming down_packed before the dual kernel has finished.
     e = nvf::launch_stream_gemv(1, h, M, I, down_packed, H, down_scale2, down_scale2, 0, out,
                                 status, w + l.down_off, l.down_bytes, sms, true, stream);
     return cuda_status(e);
@@ -198,7 +196,7 @@ nvfp4_status ffn_gate_up_nvfp4(const void* x, int M, int H, int I, const void* g
     return cuda_status(nvf::launch_stream_gemv(2, x, M, H, gate_up_packed, I, gate_scale2,
                                                up_scale2, (int)act, h, reinterpret_cast<int*>(w),
                                                w + nvf::kStatusBytes, need - nvf::kStatusBytes,
-                                               sms, false, stream));
+                                               sms, true, stream));
 }
 
 nvfp4_status nvfp4_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {

@@ -101,6 +101,9 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const void* w, int s
         *reinterpret_cast<uint2*>(codes + 8 * b) = make_uint2(word[0], word[1]);
         scales[b] = (uint8_t)s;
     }
+    // Make the codes visible GPU-wide before this block exits: the GEMV kernels
+    // may be launched as soon as every block of this grid has exited.
+    __threadfence();
 }
 
 }  // namespace

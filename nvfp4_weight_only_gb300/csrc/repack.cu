@@ -67,6 +67,9 @@ __global__ void __launch_bounds__(kThreads) repack_kernel(const uint8_t* __restr
             *reinterpret_cast<uint2*>(dst + kUnitCodeBytes + 8 * lane) = make_uint2(sw[0], sw[1]);
         }
     }
+    // Make the repacked weight visible GPU-wide before this block exits: the
+    // GEMV kernels may start streaming it as soon as every block has exited.
+    __threadfence();
 }
 
 __global__ void __launch_bounds__(kThreads) unpack_kernel(const uint8_t* __restrict__ in, int N,

@@ -47,6 +47,15 @@ constexpr int kMiscBytes = 512;
 constexpr int kFoldChunks = 8;
 // Weight units (16 rows x 64 K) each warp handles per pipeline step; a step
 // spans kUnitsPerStep / streams chunks (a divisor of kChunkAlign).
+#ifndef NVF_WEIGHT_EVICT_FIRST
+#define NVF_WEIGHT_EVICT_FIRST 0
+#endif
+// Scale application: 0 = E4M3 row scales applied to the fp32 block sums by
+// FFMA; 1 = folded into the A fragments by an exact f16 multiply (the MMAs then
+// accumulate directly) when the token rows need two n8 tiles; 2 = always.
+#ifndef NVF_SCALE_IN_A
+#define NVF_SCALE_IN_A 0
+#endif
 #ifndef NVF_UNITS_PER_STEP
 #define NVF_UNITS_PER_STEP 4
 #endif
@@ -228,32 +237,49 @@ __device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float*
     const int items = a.M * per_token;
     float mx_local = 0.0f;
     int m_local = -1;
-    for (int it = tid; it < items; it += kThreads) {
-        const int m = it / per_token, q = it - m * per_token;
-        const int ci = q >> 3, grp = q & 7;  // grp: k0 = 8*grp within the chunk
-        int c = c_start + ci;
-        if (c >= a.C) c -= a.C;
-        const int k0 = c * kChunkK + grp * 8;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (k0 < a.K) v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)m * a.K + k0));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        float mx = 0.0f;
+    // Each thread's items go in rounds of kLoads: all loads of a round are in
+    // flight together before any value is used.
+    constexpr int kLoads = 8;
+    for (int base = tid; base < items; base += kLoads * kThreads) {
+        uint4 v[kLoads];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            mx = fmaxf(mx, fabsf(__uint_as_float(w[i] << 16)));
-            mx = fmaxf(mx, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+        for (int u = 0; u < kLoads; ++u) {
+            const int it = base + u * kThreads;
+            v[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (it < items) {
+                const int m = it / per_token, q = it - m * per_token;
+                int c = c_start + (q >> 3);
+                if (c >= a.C) c -= a.C;
+                const int k0 = c * kChunkK + (q & 7) * 8;
+                if (k0 < a.K) v[u] = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)m * a.K + k0));
+            }
         }
-        // pair i (k = k0 + 2i, +1) belongs to lane quarter t = i, block j = grp/2,
-        // half = grp&1 (b0 for k%16 < 8, b1 otherwise)
-        uint8_t* base = xs + m * a.x_stride + ci * 128 + (grp >> 1) * 8 + (grp & 1) * 4;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) *reinterpret_cast<uint32_t*>(base + i * 32) = w[i];
-        if (m != m_local) {
-            if (m_local >= 0 && mx_local > 0.0f) atomicMax(&amax_u[m_local], __float_as_uint(mx_local));
-            m_local = m;
-            mx_local = 0.0f;
+        for (int u = 0; u < kLoads; ++u) {
+            const int it = base + u * kThreads;
+            if (it >= items) break;
+            const int m = it / per_token, q = it - m * per_token;
+            const int ci = q >> 3, grp = q & 7;  // grp: k0 = 8*grp within the chunk
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            float mx = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                mx = fmaxf(mx, fabsf(__uint_as_float(w[i] << 16)));
+                mx = fmaxf(mx, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+            }
+            // pair i (k = k0 + 2i, +1) belongs to lane quarter t = i, block j =
+            // grp/2, half = grp&1 (b0 for k%16 < 8, b1 otherwise)
+            uint8_t* dst = xs + m * a.x_stride + ci * 128 + (grp >> 1) * 8 + (grp & 1) * 4;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) *reinterpret_cast<uint32_t*>(dst + i * 32) = w[i];
+            if (m != m_local) {
+                if (m_local >= 0 && mx_local > 0.0f)
+                    atomicMax(&amax_u[m_local], __float_as_uint(mx_local));
+                m_local = m;
+                mx_local = 0.0f;
+            }
+            mx_local = fmaxf(mx_local, mx);
         }
-        mx_local = fmaxf(mx_local, mx);
     }
     if (m_local >= 0 && mx_local > 0.0f) atomicMax(&amax_u[m_local], __float_as_uint(mx_local));
     __syncthreads();
@@ -368,9 +394,12 @@ __device__ __forceinline__ bool finish_segment(const KArgs& a, float (&hi)[NS][N
 }
 
 // The last range to arrive for (row block rb, this warp's tile): sum every
-// range's partial in range order and store the tile's outputs.
+// range's partial in range order and store the tile's outputs.  The slot loads
+// of up to kBatch parts are all issued before any is used, so their latencies
+// overlap instead of adding up.
 template <int NS>
 __device__ __forceinline__ void reduce_tile(const KArgs& a, int rb, int warp, int lane, bool ok) {
+    constexpr int kBatch = 8;
     const long long p_lo = (long long)rb * a.CS;
     const int r_first = range_of(a, p_lo), r_last = range_of(a, p_lo + a.CS - 1);
     for (int e = lane; e < kTileRows * a.M; e += 32) {
@@ -380,13 +409,33 @@ __device__ __forceinline__ void reduce_tile(const KArgs& a, int rb, int warp, in
         float sum[NS];
 #pragma unroll
         for (int si = 0; si < NS; ++si) sum[si] = 0.0f;
-        for (int rr = r_first; rr <= r_last; ++rr) {
-            const float* sl = tile_slot<NS>(a, rr, rb, warp);
+        for (int r0 = r_first; r0 <= r_last; r0 += kBatch) {
+            float part[kBatch][NS];
 #pragma unroll
-            for (int si = 0; si < NS; ++si) sum[si] += __ldcg(sl + (si * kTileRows + row16) * a.M + token);
+            for (int b = 0; b < kBatch; ++b) {
+                const int rr = r0 + b;
+                if (rr <= r_last) {
+                    const float* sl = tile_slot<NS>(a, rr, rb, warp);
+#pragma unroll
+                    for (int si = 0; si < NS; ++si)
+                        part[b][si] = __ldcg(sl + (si * kTileRows + row16) * a.M + token);
+                } else {
+#pragma unroll
+                    for (int si = 0; si < NS; ++si) part[b][si] = 0.0f;
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b)
+#pragma unroll
+                for (int si = 0; si < NS; ++si) sum[si] += part[b][si];
         }
         if (ok) store_output<NS>(a, row, token, sum[0], sum[NS - 1]);
     }
+}
+
+template <int NT>
+__device__ __forceinline__ constexpr bool kScaleInA() {
+    return NVF_SCALE_IN_A == 2 || (NVF_SCALE_IN_A == 1 && NT == 2);
 }
 
 // One chunk (64 K elements) of the current step for this warp.  Per k16
@@ -431,24 +480,41 @@ __device__ __forceinline__ void process_chunk(const uint8_t* stage, const uint8_
         for (int jb = 0; jb < 4; ++jb) {
             uint32_t a0, a1, a2, a3;
             e2m1x8_to_f16x2x4(cws[jb], a0, a1, a2, a3);
-            const uint32_t sp = (jb & 1) ? ((jb < 2 ? sw.x : sw.y) >> 16) : (jb < 2 ? sw.x : sw.y);
-            const uint32_t s2 = e4m3x2_to_f16x2(sp);  // (row g, row g+8) scales
-            const float sg = __half2float(__ushort_as_half((unsigned short)(s2 & 0xFFFFu)));
-            const float sg8 = __half2float(__ushort_as_half((unsigned short)(s2 >> 16)));
+            const uint32_t sword = jb < 2 ? sw.x : sw.y;
+            if (kScaleInA<NT>()) {
+                // (s_g, s_g) and (s_g8, s_g8) as f16x2: E4M3 x E2M1 is exact in f16
+                const uint32_t bsel = 2 * (jb & 1);
+                const uint32_t sg = e4m3x2_to_f16x2(prmt(sword, 0u, bsel | (bsel << 4)));
+                const uint32_t sg8 = e4m3x2_to_f16x2(prmt(sword, 0u, (bsel + 1) | ((bsel + 1) << 4)));
+                a0 = hmul2(a0, sg);
+                a2 = hmul2(a2, sg);
+                a1 = hmul2(a1, sg8);
+                a3 = hmul2(a3, sg8);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                mma_f16_16816(d, a0, a1, a2, a3, b[nt][2 * jb], b[nt][2 * jb + 1]);
-                acc[si][nt][0] = fmaf(d[0], sg, acc[si][nt][0]);
-                acc[si][nt][1] = fmaf(d[1], sg, acc[si][nt][1]);
-                acc[si][nt][2] = fmaf(d[2], sg8, acc[si][nt][2]);
-                acc[si][nt][3] = fmaf(d[3], sg8, acc[si][nt][3]);
+                for (int nt = 0; nt < NT; ++nt)
+                    mma_f16_16816(acc[si][nt], a0, a1, a2, a3, b[nt][2 * jb], b[nt][2 * jb + 1]);
+            } else {
+                const uint32_t sp = (jb & 1) ? (sword >> 16) : sword;
+                const uint32_t s2 = e4m3x2_to_f16x2(sp);  // (row g, row g+8) scales
+                const float sgf = __half2float(__ushort_as_half((unsigned short)(s2 & 0xFFFFu)));
+                const float sg8f = __half2float(__ushort_as_half((unsigned short)(s2 >> 16)));
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    mma_f16_16816(d, a0, a1, a2, a3, b[nt][2 * jb], b[nt][2 * jb + 1]);
+                    acc[si][nt][0] = fmaf(d[0], sgf, acc[si][nt][0]);
+                    acc[si][nt][1] = fmaf(d[1], sgf, acc[si][nt][1]);
+                    acc[si][nt][2] = fmaf(d[2], sg8f, acc[si][nt][2]);
+                    acc[si][nt][3] = fmaf(d[3], sg8f, acc[si][nt][3]);
+                }
             }
         }
     }
 }
 
 // Issue the bulk copy of the step at `cur` into ring stage st (one thread).
+// The weights are read exactly once per call, so their lines are marked for
+// early eviction: L2 keeps the token rows, h and the split-K partials instead.
 template <int NS>
 __device__ __forceinline__ void issue_step(const KArgs& a, const StepCursor& cur, int st,
                                            uint32_t ring_s, uint32_t full0, int* issues) {
@@ -456,9 +522,15 @@ __device__ __forceinline__ void issue_step(const KArgs& a, const StepCursor& cur
     constexpr int CPS = kUnitsPerStep / NS;
     const uint32_t bytes = (uint32_t)(CPS * kBlockTiles * UB);
     mbar_arrive_expect_tx(full0 + 8u * st, bytes);
+#if NVF_WEIGHT_EVICT_FIRST
+    bulk_copy_g2s_hint(ring_s + (uint32_t)(st * a.stage_bytes),
+                       a.blob + ((size_t)cur.rb * a.C + (size_t)cur.cb * CPS) * kBlockTiles * UB,
+                       bytes, full0 + 8u * st, l2_evict_first_policy());
+#else
     bulk_copy_g2s(ring_s + (uint32_t)(st * a.stage_bytes),
                   a.blob + ((size_t)cur.rb * a.C + (size_t)cur.cb * CPS) * kBlockTiles * UB, bytes,
                   full0 + 8u * st);
+#endif
     ++issues[st];
 }
 
