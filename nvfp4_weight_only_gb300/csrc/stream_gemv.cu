@@ -48,13 +48,13 @@ constexpr int kFoldChunks = 8;
 // Weight units (16 rows x 64 K) each warp handles per pipeline step; a step
 // spans kUnitsPerStep / streams chunks (a divisor of kChunkAlign).
 #ifndef NVF_WEIGHT_EVICT_FIRST
-#define NVF_WEIGHT_EVICT_FIRST 0
+#define NVF_WEIGHT_EVICT_FIRST 1
 #endif
 // Scale application: 0 = E4M3 row scales applied to the fp32 block sums by
 // FFMA; 1 = folded into the A fragments by an exact f16 multiply (the MMAs then
 // accumulate directly) when the token rows need two n8 tiles; 2 = always.
 #ifndef NVF_SCALE_IN_A
-#define NVF_SCALE_IN_A 0
+#define NVF_SCALE_IN_A 1
 #endif
 #ifndef NVF_UNITS_PER_STEP
 #define NVF_UNITS_PER_STEP 4
@@ -394,42 +394,50 @@ __device__ __forceinline__ bool finish_segment(const KArgs& a, float (&hi)[NS][N
 }
 
 // The last range to arrive for (row block rb, this warp's tile): sum every
-// range's partial in range order and store the tile's outputs.  The slot loads
-// of up to kBatch parts are all issued before any is used, so their latencies
-// overlap instead of adding up.
+// range's partial in range order and store the tile's outputs.  Each lane owns
+// up to kIter of the tile's 16 x M elements; the slot loads of all of them for
+// kB ranges are issued before any is used, so a tile costs one load latency
+// per kB ranges whatever M is.
 template <int NS>
 __device__ __forceinline__ void reduce_tile(const KArgs& a, int rb, int warp, int lane, bool ok) {
-    constexpr int kBatch = 8;
+    constexpr int kIter = kTileRows * 16 / 32;  // elements per lane at M = 16
+    constexpr int kB = 4 / NS;                  // ranges per batch
     const long long p_lo = (long long)rb * a.CS;
     const int r_first = range_of(a, p_lo), r_last = range_of(a, p_lo + a.CS - 1);
-    for (int e = lane; e < kTileRows * a.M; e += 32) {
+    const int n_el = kTileRows * a.M;
+    float sum[kIter][NS];
+#pragma unroll
+    for (int i = 0; i < kIter; ++i)
+#pragma unroll
+        for (int si = 0; si < NS; ++si) sum[i][si] = 0.0f;
+    for (int r0 = r_first; r0 <= r_last; r0 += kB) {
+        float part[kB][kIter][NS];
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+            const int rr = r0 + b;
+            const float* sl = rr <= r_last ? tile_slot<NS>(a, rr, rb, warp) : nullptr;
+#pragma unroll
+            for (int i = 0; i < kIter; ++i) {
+                const int e = lane + 32 * i;
+#pragma unroll
+                for (int si = 0; si < NS; ++si)
+                    part[b][i][si] = (sl != nullptr && e < n_el) ? __ldcg(sl + si * n_el + e) : 0.0f;
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kB; ++b)
+#pragma unroll
+            for (int i = 0; i < kIter; ++i)
+#pragma unroll
+                for (int si = 0; si < NS; ++si) sum[i][si] += part[b][i][si];
+    }
+#pragma unroll
+    for (int i = 0; i < kIter; ++i) {
+        const int e = lane + 32 * i;
+        if (e >= n_el) continue;
         const int token = e % a.M, row16 = e / a.M;
         const int row = rb * kBlockRows + warp * kTileRows + row16;
-        if (row >= a.N) continue;
-        float sum[NS];
-#pragma unroll
-        for (int si = 0; si < NS; ++si) sum[si] = 0.0f;
-        for (int r0 = r_first; r0 <= r_last; r0 += kBatch) {
-            float part[kBatch][NS];
-#pragma unroll
-            for (int b = 0; b < kBatch; ++b) {
-                const int rr = r0 + b;
-                if (rr <= r_last) {
-                    const float* sl = tile_slot<NS>(a, rr, rb, warp);
-#pragma unroll
-                    for (int si = 0; si < NS; ++si)
-                        part[b][si] = __ldcg(sl + (si * kTileRows + row16) * a.M + token);
-                } else {
-#pragma unroll
-                    for (int si = 0; si < NS; ++si) part[b][si] = 0.0f;
-                }
-            }
-#pragma unroll
-            for (int b = 0; b < kBatch; ++b)
-#pragma unroll
-                for (int si = 0; si < NS; ++si) sum[si] += part[b][si];
-        }
-        if (ok) store_output<NS>(a, row, token, sum[0], sum[NS - 1]);
+        if (ok && row < a.N) store_output<NS>(a, row, token, sum[i][0], sum[i][NS - 1]);
     }
 }
 
@@ -481,11 +489,14 @@ __device__ __forceinline__ void process_chunk(const uint8_t* stage, const uint8_
             uint32_t a0, a1, a2, a3;
             e2m1x8_to_f16x2x4(cws[jb], a0, a1, a2, a3);
             const uint32_t sword = jb < 2 ? sw.x : sw.y;
+            const uint32_t sp = (jb & 1) ? (sword >> 16) : sword;
+            const uint32_t s2 = e4m3x2_to_f16x2(sp);  // (row g, row g+8) scales
             if (kScaleInA<NT>()) {
-                // (s_g, s_g) and (s_g8, s_g8) as f16x2: E4M3 x E2M1 is exact in f16
-                const uint32_t bsel = 2 * (jb & 1);
-                const uint32_t sg = e4m3x2_to_f16x2(prmt(sword, 0u, bsel | (bsel << 4)));
-                const uint32_t sg8 = e4m3x2_to_f16x2(prmt(sword, 0u, (bsel + 1) | ((bsel + 1) << 4)));
+                // (s_g, s_g) and (s_g8, s_g8) as f16x2; an E4M3 value times an
+                // E2M1 value is exact in f16 (at most 6 significant bits,
+                // magnitudes from 2^-10 to 2688).
+                const uint32_t sg = prmt(s2, 0u, 0x1010u);
+                const uint32_t sg8 = prmt(s2, 0u, 0x3232u);
                 a0 = hmul2(a0, sg);
                 a2 = hmul2(a2, sg);
                 a1 = hmul2(a1, sg8);
@@ -494,8 +505,6 @@ __device__ __forceinline__ void process_chunk(const uint8_t* stage, const uint8_
                 for (int nt = 0; nt < NT; ++nt)
                     mma_f16_16816(acc[si][nt], a0, a1, a2, a3, b[nt][2 * jb], b[nt][2 * jb + 1]);
             } else {
-                const uint32_t sp = (jb & 1) ? (sword >> 16) : sword;
-                const uint32_t s2 = e4m3x2_to_f16x2(sp);  // (row g, row g+8) scales
                 const float sgf = __half2float(__ushort_as_half((unsigned short)(s2 & 0xFFFFu)));
                 const float sg8f = __half2float(__ushort_as_half((unsigned short)(s2 >> 16)));
 #pragma unroll
