@@ -102,8 +102,8 @@ nvfp4_status nvfp4_quantize(const void* w, nvfp4_src_dtype dtype, int N, int K,
 /*
  * Kernel layout ("fragment layout"): a byte permutation of the canonical codes
  * and scales (the principle of DenseFfnLayer::ensure_nvfp4_mmq_weight: same
- * codes, same scale bytes, no numerics), zero-padded to N' = roundup(N, 128)
- * rows and K' = roundup(K, 64) columns.  For N % 128 == 0 and K % 64 == 0 it
+ * codes, same scale bytes, no numerics), zero-padded to N' = roundup(N, 256)
+ * rows and K' = roundup(K, 256) columns.  For N % 256 == 0 and K % 256 == 0 it
  * holds exactly the canonical byte count N*K*9/16.  The layout is opaque to
  * callers; nvfp4_unpack inverts it.
  */

@@ -47,15 +47,6 @@ constexpr int kMiscBytes = 512;
 constexpr int kFoldChunks = 8;
 // Weight units (16 rows x 64 K) each warp handles per pipeline step; a step
 // spans kUnitsPerStep / streams chunks (a divisor of kChunkAlign).
-#ifndef NVF_WEIGHT_EVICT_FIRST
-#define NVF_WEIGHT_EVICT_FIRST 1
-#endif
-// Scale application: 0 = E4M3 row scales applied to the fp32 block sums by
-// FFMA; 1 = folded into the A fragments by an exact f16 multiply (the MMAs then
-// accumulate directly) when the token rows need two n8 tiles; 2 = always.
-#ifndef NVF_SCALE_IN_A
-#define NVF_SCALE_IN_A 1
-#endif
 #ifndef NVF_UNITS_PER_STEP
 #define NVF_UNITS_PER_STEP 4
 #endif
@@ -398,10 +389,10 @@ __device__ __forceinline__ bool finish_segment(const KArgs& a, float (&hi)[NS][N
 // up to kIter of the tile's 16 x M elements; the slot loads of all of them for
 // kB ranges are issued before any is used, so a tile costs one load latency
 // per kB ranges whatever M is.
-template <int NS>
+template <int NS, int NT>
 __device__ __forceinline__ void reduce_tile(const KArgs& a, int rb, int warp, int lane, bool ok) {
-    constexpr int kIter = kTileRows * 16 / 32;  // elements per lane at M = 16
-    constexpr int kB = 4 / NS;                  // ranges per batch
+    constexpr int kIter = kTileRows * 8 * NT / 32;  // elements per lane at M = 8 NT
+    constexpr int kB = 32 / (kIter * NS);           // ranges per batch (32 loads in flight)
     const long long p_lo = (long long)rb * a.CS;
     const int r_first = range_of(a, p_lo), r_last = range_of(a, p_lo + a.CS - 1);
     const int n_el = kTileRows * a.M;
@@ -441,9 +432,14 @@ __device__ __forceinline__ void reduce_tile(const KArgs& a, int rb, int warp, in
     }
 }
 
+// Where the E4M3 row scales are applied.  With one n8 token tile: to the fp32
+// block sums of independent zero-initialised MMAs, by FFMA (measured faster
+// than chained MMAs on GB300).  With two token tiles: folded into the A
+// fragments by an exact f16 multiply, so the MMAs accumulate directly and the
+// scaling is shared by both tiles.
 template <int NT>
 __device__ __forceinline__ constexpr bool kScaleInA() {
-    return NVF_SCALE_IN_A == 2 || (NVF_SCALE_IN_A == 1 && NT == 2);
+    return NT == 2;
 }
 
 // One chunk (64 K elements) of the current step for this warp.  Per k16
@@ -452,7 +448,7 @@ __device__ __forceinline__ constexpr bool kScaleInA() {
 // a zero accumulator, and the two row scales (E4M3 -> f16 -> f32, exact) are
 // applied to those fp32 block sums with FFMAs.  Every MMA is independent; the
 // FMA pipe takes the scaling, which leaves the ALU pipe to the decode.
-template <int NS, int NT>
+template <int NS, int NT, bool ONE>
 __device__ __forceinline__ void process_chunk(const uint8_t* stage, const uint8_t* xs,
                                               int x_stride, int M, int j, int cj, int warp,
                                               int lane, float (&acc)[NS][NT][4]) {
@@ -512,13 +508,23 @@ __device__ __forceinline__ void process_chunk(const uint8_t* stage, const uint8_
                     float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                     mma_f16_16816(d, a0, a1, a2, a3, b[nt][2 * jb], b[nt][2 * jb + 1]);
                     acc[si][nt][0] = fmaf(d[0], sgf, acc[si][nt][0]);
-                    acc[si][nt][1] = fmaf(d[1], sgf, acc[si][nt][1]);
                     acc[si][nt][2] = fmaf(d[2], sg8f, acc[si][nt][2]);
-                    acc[si][nt][3] = fmaf(d[3], sg8f, acc[si][nt][3]);
+                    if (!ONE) {  // columns 2t+1 hold token 1 and up
+                        acc[si][nt][1] = fmaf(d[1], sgf, acc[si][nt][1]);
+                        acc[si][nt][3] = fmaf(d[3], sg8f, acc[si][nt][3]);
+                    }
                 }
             }
         }
     }
+}
+
+// First byte of the step at `cur` in the repacked blob.
+template <int NS>
+__device__ __forceinline__ const uint8_t* step_src(const KArgs& a, const StepCursor& cur) {
+    constexpr int UB = kUnitBytes * NS;
+    constexpr int CPS = kUnitsPerStep / NS;
+    return a.blob + ((size_t)cur.rb * a.C + (size_t)cur.cb * CPS) * kBlockTiles * UB;
 }
 
 // Issue the bulk copy of the step at `cur` into ring stage st (one thread).
@@ -531,19 +537,13 @@ __device__ __forceinline__ void issue_step(const KArgs& a, const StepCursor& cur
     constexpr int CPS = kUnitsPerStep / NS;
     const uint32_t bytes = (uint32_t)(CPS * kBlockTiles * UB);
     mbar_arrive_expect_tx(full0 + 8u * st, bytes);
-#if NVF_WEIGHT_EVICT_FIRST
-    bulk_copy_g2s_hint(ring_s + (uint32_t)(st * a.stage_bytes),
-                       a.blob + ((size_t)cur.rb * a.C + (size_t)cur.cb * CPS) * kBlockTiles * UB,
-                       bytes, full0 + 8u * st, l2_evict_first_policy());
-#else
-    bulk_copy_g2s(ring_s + (uint32_t)(st * a.stage_bytes),
-                  a.blob + ((size_t)cur.rb * a.C + (size_t)cur.cb * CPS) * kBlockTiles * UB, bytes,
-                  full0 + 8u * st);
-#endif
+    bulk_copy_g2s_hint(ring_s + (uint32_t)(st * a.stage_bytes), step_src<NS>(a, cur), bytes,
+                       full0 + 8u * st, l2_evict_first_policy());
     ++issues[st];
 }
 
-template <int NS, int NT>
+// ONE: a single token row (M == 1), which needs only the even MMA columns.
+template <int NS, int NT, bool ONE>
 __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a) {
     constexpr int CPS = kUnitsPerStep / NS;  // chunks per step
 
@@ -642,7 +642,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
                 const uint8_t* stage = smem + (size_t)st * a.stage_bytes;
 #pragma unroll
                 for (int j = 0; j < CPS; ++j)
-                    process_chunk<NS, NT>(stage, xs, a.x_stride, a.M, j, ci + j, warp, lane, acc);
+                    process_chunk<NS, NT, ONE>(stage, xs, a.x_stride, a.M, j, ci + j, warp, lane,
+                                               acc);
             }
             // Release the stage; the last warp out refills it a ring ahead.
             __syncwarp();
@@ -676,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
+                        for (int e = 0; e < 4; e += ONE ? 2 : 1) {
                             two_sum_acc(hi[si][nt][e], lo[si][nt][e], acc[si][nt][e]);
                             acc[si][nt][e] = 0.0f;
                         }
@@ -686,11 +687,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
                 if (n_pending < kMaxPending)
                     pending[n_pending++] = rb_now;
                 else
-                    reduce_tile<NS>(a, rb_now, warp, lane, ok);
+                    reduce_tile<NS, NT>(a, rb_now, warp, lane, ok);
             }
         }
     }
-    for (int i = 0; i < n_pending; ++i) reduce_tile<NS>(a, pending[i], warp, lane, ok);
+    for (int i = 0; i < n_pending; ++i) reduce_tile<NS, NT>(a, pending[i], warp, lane, ok);
     // A CTA that abandoned a wait still owns copies in flight: wait for them
     // (bounded) before the shared memory is released.
     __syncthreads();
@@ -724,13 +725,13 @@ size_t gemv_scratch_bytes(int streams, int M, int N, int K, int num_sms) {
     return make_plan(streams, M, N, K, num_sms).total;
 }
 
-template <int NS, int NT>
+template <int NS, int NT, bool ONE>
 static cudaError_t launch_t(const Plan& p, const KArgs& a, cudaStream_t s) {
     static bool attr_done[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(stream_gemv_kernel<NS, NT>,
+        cudaError_t e = cudaFuncSetAttribute(stream_gemv_kernel<NS, NT, ONE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
@@ -745,7 +746,7 @@ static cudaError_t launch_t(const Plan& p, const KArgs& a, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, stream_gemv_kernel<NS, NT>, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, stream_gemv_kernel<NS, NT, ONE>, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -784,9 +785,12 @@ cudaError_t launch_stream_gemv(int streams, const void* x, int M, int K, const v
     a.scale_b = scale_b;
     a.act = act;
     a.early_weights = early_weights ? 1 : 0;
-    if (streams == 1)
-        return p.NT == 1 ? launch_t<1, 1>(p, a, s) : launch_t<1, 2>(p, a, s);
-    return p.NT == 1 ? launch_t<2, 1>(p, a, s) : launch_t<2, 2>(p, a, s);
+    if (streams == 1) {
+        if (M == 1) return launch_t<1, 1, true>(p, a, s);
+        return p.NT == 1 ? launch_t<1, 1, false>(p, a, s) : launch_t<1, 2, false>(p, a, s);
+    }
+    if (M == 1) return launch_t<2, 1, true>(p, a, s);
+    return p.NT == 1 ? launch_t<2, 1, false>(p, a, s) : launch_t<2, 2, false>(p, a, s);
 }
 
 }  // namespace nvf
