@@ -111,6 +111,24 @@ static Plan make_plan(int NS, int M, int N, int K, int num_sms) {
     return p;
 }
 
+// Division by a fixed divisor d >= 1 of numerators below 2^32, by a multiply:
+// with m = floor((2^64 - 1) / d) + 1, floor(n / d) = high 64 bits of n * m for
+// every n < 2^32 (the product overshoots n / d by less than n / 2^64 < 1 / d,
+// which never crosses the next integer).  d == 1 is passed through.
+struct FastDiv {
+    unsigned long long m;
+    unsigned d;
+    static FastDiv make(unsigned d) {
+        FastDiv f;
+        f.d = d;
+        f.m = d > 1 ? ~0ull / d + 1 : 0;
+        return f;
+    }
+    __device__ __forceinline__ unsigned div(unsigned n) const {
+        return d > 1 ? (unsigned)__umul64hi((unsigned long long)n, m) : n;
+    }
+};
+
 struct KArgs {
     const __nv_bfloat16* x;
     const uint8_t* blob;
@@ -124,15 +142,25 @@ struct KArgs {
     float scale_a, scale_b;
     int act;
     int early_weights;  // stream weights before waiting on the preceding kernel
+    // L * R < 2^32: the range arithmetic below runs on FastDiv multiplies
+    int fast;
+    FastDiv div_R, div_L, div_CS;
 };
 
 __device__ __forceinline__ long long range_start(const KArgs& a, long long r) {
+    if (a.fast) return a.div_R.div((unsigned)(r * a.L));
     return r * a.L / a.R;
 }
 
 // Index of the range that contains step q (inverse of range_start).
 __device__ __forceinline__ int range_of(const KArgs& a, long long q) {
+    if (a.fast) return (int)a.div_L.div((unsigned)((q + 1) * a.R - 1));
     return (int)(((q + 1) * (long long)a.R - 1) / a.L);
+}
+
+// Row block of step q.
+__device__ __forceinline__ int rb_of_step(const KArgs& a, int q) {
+    return a.fast ? (int)a.div_CS.div((unsigned)q) : q / a.CS;
 }
 
 // Position in this CTA's step sequence: ranges blockIdx.x, +grid, +2*grid, ...
@@ -142,8 +170,8 @@ struct StepCursor {
         if (r < a.R) {
             q = (int)range_start(a, r);
             q_end = (int)range_start(a, r + 1);
-            rb = q / a.CS;
-            cb = q % a.CS;
+            rb = rb_of_step(a, q);
+            cb = q - rb * a.CS;
         }
     }
     __device__ __forceinline__ void init(const KArgs& a) {
@@ -308,7 +336,7 @@ __device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float*
 template <int NS>
 __device__ __forceinline__ float* tile_slot(const KArgs& a, int r, int rb, int warp) {
     const size_t slot = (size_t)kBlockTiles * NS * kTileRows * a.M;
-    const int si_slot = rb - (int)(range_start(a, r) / a.CS);
+    const int si_slot = rb - rb_of_step(a, (int)range_start(a, r));
     return a.partials + ((size_t)r * a.s_max + si_slot) * slot + (size_t)warp * NS * kTileRows * a.M;
 }
 
@@ -785,6 +813,10 @@ cudaError_t launch_stream_gemv(int streams, const void* x, int M, int K, const v
     a.scale_b = scale_b;
     a.act = act;
     a.early_weights = early_weights ? 1 : 0;
+    a.fast = (unsigned long long)p.L * (unsigned long long)p.R < (1ull << 32) ? 1 : 0;
+    a.div_R = FastDiv::make((unsigned)p.R);
+    a.div_L = FastDiv::make((unsigned)(p.L < (1LL << 32) ? p.L : 1));
+    a.div_CS = FastDiv::make((unsigned)p.CS);
     if (streams == 1) {
         if (M == 1) return launch_t<1, 1, true>(p, a, s);
         return p.NT == 1 ? launch_t<1, 1, false>(p, a, s) : launch_t<1, 2, false>(p, a, s);
