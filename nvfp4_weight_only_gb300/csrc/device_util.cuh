@@ -136,6 +136,17 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D = A * B for one m16n8k16 tile from a zero accumulator (C is the constant
+// 0, D is write-only, so no accumulator registers need clearing).
+__device__ __forceinline__ void mma_f16_16816_zero(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                   uint32_t a2, uint32_t a3, uint32_t b0,
+                                                   uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
 // Round-to-nearest-even, saturating conversion of one fp32 to an E4M3 byte.
 __device__ __forceinline__ uint32_t f32_to_e4m3(float v) {
     uint16_t r;

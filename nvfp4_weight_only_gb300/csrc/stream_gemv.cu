@@ -76,7 +76,9 @@ static Plan make_plan(int NS, int M, int N, int K, int num_sms) {
     // x lives in shared memory as f16, token-major: per token 128 bytes per
     // chunk (+16 bytes of row padding that keeps the B-fragment loads free of
     // bank conflicts).
-    const int xcap_max = (kXBudget - 16 * M) / (128 * M);
+    // M <= 2 uses the diagonal layout: 1024 bytes per chunk for both tokens.
+    const bool diag = M <= 2;
+    const int xcap_max = diag ? kXBudget / 1024 : (kXBudget - 16 * M) / (128 * M);
     p.grid = num_sms > 0 ? num_sms : 1;
     if (p.L < p.grid) p.grid = (int)p.L;
     for (int rpc = 1;; ++rpc) {
@@ -88,9 +90,9 @@ static Plan make_plan(int NS, int M, int N, int K, int num_sms) {
         if (need <= xcap_max || p.R == p.L) break;
     }
     p.xcap = (int)(p.Pmax * p.cps < p.C ? p.Pmax * p.cps : p.C);
-    p.x_stride = p.xcap * 128 + 16;
+    p.x_stride = diag ? 0 : p.xcap * 128 + 16;
     p.stage_bytes = p.cps * kBlockTiles * kUnitBytes * NS;
-    const int x_bytes = M * p.x_stride;
+    const int x_bytes = diag ? p.xcap * 1024 : M * p.x_stride;
     int ring = kSmemMax - x_bytes - kMiscBytes - 32 * kMaxStages - 256;
     if (ring > kRingBudget) ring = kRingBudget;
     p.stages = ring / p.stage_bytes;
@@ -238,6 +240,33 @@ __device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float b) {
     lo += err;
 }
 
+// Per token m (threads 0..15): the exponent e_m with amax_m * 2^e_m in
+// [2^14, 2^15), kept biased in amax_u[m] for the conversion pass, and the
+// unscale factor 2^-e_m for the fp32 results.
+__device__ __forceinline__ void token_scales(unsigned* amax_u, float* tok_unscale) {
+    const int tid = threadIdx.x;
+    if (tid < 16) {
+        const float am = __uint_as_float(amax_u[tid]);
+        int e = 0;
+        if (am > 0.0f) {
+            int ex;
+            frexpf(am, &ex);  // am < 2^ex, so am * 2^(15-ex) lies in [2^14, 2^15)
+            e = 15 - ex;
+            e = e < -100 ? -100 : (e > 100 ? 100 : e);
+        }
+        amax_u[tid] = (unsigned)(e + 128);  // reuse: biased exponent for the second pass
+        tok_unscale[tid] = __int_as_float((127 - e) << 23);
+    }
+}
+
+// bf16 pair -> f16 pair scaled by 2^(biased - 128) (exact for the range kept).
+__device__ __forceinline__ uint32_t scale_pair_to_f16(uint32_t pr, unsigned biased) {
+    const float sc = __int_as_float(((int)biased - 128 + 127) << 23);
+    const __half2 hv = __floats2half2_rn(__uint_as_float(pr << 16) * sc,
+                                         __uint_as_float(pr & 0xFFFF0000u) * sc);
+    return *reinterpret_cast<const uint32_t*>(&hv);
+}
+
 // Stage the token rows for chunks c_start .. c_start+nx-1 (mod C) into shared
 // memory as f16, token-major, in the order the B fragments are read: for token
 // m and chunk ci, 128 bytes at m*x_stride + ci*128, where lane quarter t owns
@@ -302,30 +331,81 @@ __device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float*
     }
     if (m_local >= 0 && mx_local > 0.0f) atomicMax(&amax_u[m_local], __float_as_uint(mx_local));
     __syncthreads();
-    if (tid < 16) {
-        const float am = __uint_as_float(amax_u[tid]);
-        int e = 0;
-        if (am > 0.0f) {
-            int ex;
-            frexpf(am, &ex);  // am < 2^ex, so am * 2^(15-ex) lies in [2^14, 2^15)
-            e = 15 - ex;
-            e = e < -100 ? -100 : (e > 100 ? 100 : e);
-        }
-        amax_u[tid] = (unsigned)(e + 128);  // reuse: biased exponent for the second pass
-        tok_unscale[tid] = __int_as_float((127 - e) << 23);
-    }
+    token_scales(amax_u, tok_unscale);
     __syncthreads();
     const int words = a.M * nx * 32;  // 32-bit words (bf16 pairs) to convert
     for (int it = tid; it < words; it += kThreads) {
         const int m = it / (nx * 32), wi = it - m * (nx * 32);
         uint32_t* p = reinterpret_cast<uint32_t*>(xs + m * a.x_stride) + wi;
-        const float sc = __int_as_float(((int)amax_u[m] - 128 + 127) << 23);
-        const uint32_t pr = *p;
-        const __half2 hv = __floats2half2_rn(__uint_as_float(pr << 16) * sc,
-                                             __uint_as_float(pr & 0xFFFF0000u) * sc);
-        *p = *reinterpret_cast<const uint32_t*>(&hv);
+        *p = scale_pair_to_f16(*p, amax_u[m]);
     }
     (void)lane;
+    __syncthreads();
+}
+
+// Token rows for one or two tokens ("diagonal" B operand).  The 8 columns of
+// an m16n8k16 tile hold (scale block j of the chunk, token m) at column
+// 2j + m: the MMA of block j sees the token rows only in its own two columns,
+// so the four MMAs of a chunk can accumulate into one tile and lane quarter t
+// ends up holding block t's sums, which it alone scales.  Per chunk ci the
+// 1024 bytes at ci*1024 hold, for lane L = 4g + t, the B registers of the four
+// MMAs: bytes h*512 + 16L + 4r (h = j/2, r = 2(j%2) + b) are the pair
+// (x[m][16j + 2t + 8b], +1) when g = 2j + m with m < M, and zero otherwise.
+// Same two passes as stage_x (coalesced load + scatter + amax, then an exact
+// power-of-two f16 conversion), after a zero fill of the chunks.
+__device__ void stage_x_diag(const KArgs& a, uint8_t* xs, int c_start, int nx, float* tok_unscale,
+                             unsigned* amax_u) {
+    const int tid = threadIdx.x;
+    if (tid < 16) amax_u[tid] = 0u;
+    for (int i = tid; i < nx * 64; i += kThreads)
+        reinterpret_cast<uint4*>(xs)[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    const int per_token = nx * 8;  // 16-byte groups of 8 k per token
+    const int items = a.M * per_token;
+    float mx_local = 0.0f;
+    int m_local = -1;
+    for (int it = tid; it < items; it += kThreads) {
+        const int m = it / per_token, q = it - m * per_token;
+        const int ci = q >> 3, grp = q & 7;  // k0 = 8*grp within the chunk
+        int c = c_start + ci;
+        if (c >= a.C) c -= a.C;
+        const int k0 = c * kChunkK + grp * 8;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (k0 < a.K) v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)m * a.K + k0));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        float mx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            mx = fmaxf(mx, fabsf(__uint_as_float(w[i] << 16)));
+            mx = fmaxf(mx, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+        }
+        // pair i (k = 8*grp + 2i): block j = grp/2, half b = grp&1, quarter t = i
+        const int j = grp >> 1, b = grp & 1;
+        uint8_t* dst = xs + ci * 1024 + (j >> 1) * 512 + (4 * (2 * j + m)) * 16 + 4 * (2 * (j & 1) + b);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) *reinterpret_cast<uint32_t*>(dst + 16 * i) = w[i];
+        if (m != m_local) {
+            if (m_local >= 0 && mx_local > 0.0f)
+                atomicMax(&amax_u[m_local], __float_as_uint(mx_local));
+            m_local = m;
+            mx_local = 0.0f;
+        }
+        mx_local = fmaxf(mx_local, mx);
+    }
+    if (m_local >= 0 && mx_local > 0.0f) atomicMax(&amax_u[m_local], __float_as_uint(mx_local));
+    __syncthreads();
+    token_scales(amax_u, tok_unscale);
+    __syncthreads();
+    // convert the M*32 non-zero words of every chunk: (m, j, t, b)
+    const int words = nx * a.M * 32;
+    for (int it = tid; it < words; it += kThreads) {
+        const int ci = it / (a.M * 32), rem = it - ci * (a.M * 32);
+        const int m = rem >> 5, w5 = rem & 31;
+        const int j = w5 >> 3, t = (w5 >> 1) & 3, b = w5 & 1;
+        uint32_t* p = reinterpret_cast<uint32_t*>(xs + ci * 1024 + (j >> 1) * 512 +
+                                                  (4 * (2 * j + m) + t) * 16 + 4 * (2 * (j & 1) + b));
+        *p = scale_pair_to_f16(*p, amax_u[m]);
+    }
     __syncthreads();
 }
 
@@ -365,7 +445,7 @@ __device__ __forceinline__ bool publish_tile(const KArgs& a, int rb, int warp, i
 // range's slot, is published (fence, then the tile's counter), and the
 // function returns true when this range arrived last for the tile and must
 // reduce it (done after the stream, by reduce_tile).
-template <int NS, int NT>
+template <int NS, int NT, bool DIAG>
 __device__ __forceinline__ bool finish_segment(const KArgs& a, float (&hi)[NS][NT][4],
                                                float (&lo)[NS][NT][4],
                                                const float (&unscale)[NT][2], int r, int q0,
@@ -383,15 +463,23 @@ __device__ __forceinline__ bool finish_segment(const KArgs& a, float (&hi)[NS][N
                 v[si][nt][e] = (hi[si][nt][e] + lo[si][nt][e]) * unscale[nt][e & 1];
                 hi[si][nt][e] = 0.0f;
                 lo[si][nt][e] = 0.0f;
+                if (DIAG) {  // lane quarters hold blocks 0..3: sum them (fixed order)
+                    v[si][nt][e] += __shfl_xor_sync(0xffffffffu, v[si][nt][e], 1);
+                    v[si][nt][e] += __shfl_xor_sync(0xffffffffu, v[si][nt][e], 2);
+                }
             }
+    // Element e of lane (g, tq) is row g + 8*(e>>1) and token nt*8 + 2*tq + (e&1);
+    // with the diagonal layout every quarter holds the same sums, token e&1,
+    // and quarter 0 stores them.
+    const bool lane_stores = !DIAG || tq == 0;
     if (full_cover) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int row = rb * kBlockRows + warp * kTileRows + g + 8 * (e >> 1);
-                const int token = nt * 8 + 2 * tq + (e & 1);
-                if (ok && row < a.N && token < a.M)
+                const int token = DIAG ? (e & 1) : nt * 8 + 2 * tq + (e & 1);
+                if (ok && lane_stores && row < a.N && token < a.M)
                     store_output<NS>(a, row, token, v[0][nt][e], v[NS - 1][nt][e]);
             }
         return false;
@@ -403,8 +491,8 @@ __device__ __forceinline__ bool finish_segment(const KArgs& a, float (&hi)[NS][N
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int token = nt * 8 + 2 * tq + (e & 1);
-                if (token < a.M)
+                const int token = DIAG ? (e & 1) : nt * 8 + 2 * tq + (e & 1);
+                if (lane_stores && token < a.M)
                     slot[(si * kTileRows + g + 8 * (e >> 1)) * a.M + token] = v[si][nt][e];
             }
     __threadfence();
@@ -533,8 +621,8 @@ __device__ __forceinline__ void process_chunk(const uint8_t* stage, const uint8_
                 const float sg8f = __half2float(__ushort_as_half((unsigned short)(s2 >> 16)));
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                    mma_f16_16816(d, a0, a1, a2, a3, b[nt][2 * jb], b[nt][2 * jb + 1]);
+                    float d[4];
+                    mma_f16_16816_zero(d, a0, a1, a2, a3, b[nt][2 * jb], b[nt][2 * jb + 1]);
                     acc[si][nt][0] = fmaf(d[0], sgf, acc[si][nt][0]);
                     acc[si][nt][2] = fmaf(d[2], sg8f, acc[si][nt][2]);
                     if (!ONE) {  // columns 2t+1 hold token 1 and up
@@ -543,6 +631,50 @@ __device__ __forceinline__ void process_chunk(const uint8_t* stage, const uint8_
                     }
                 }
             }
+        }
+    }
+}
+
+// One chunk with the diagonal token layout (M <= 2, stage_x_diag): the four
+// MMAs of the chunk accumulate into one tile, whose columns 2j, 2j+1 hold
+// block j's sums for tokens 0, 1; lane quarter t then applies block t's two
+// row scales (rows g, g+8) with FFMAs.  Per k16 block: 4 cvt + 1 MMA; per
+// chunk and lane: one scale-pair select and conversion and 2 (ONE) or 4 FFMAs.
+template <int NS, bool ONE>
+__device__ __forceinline__ void process_chunk_diag(const uint8_t* stage, const uint8_t* xs, int j,
+                                                   int cj, int warp, int lane, uint32_t scale_sel,
+                                                   float (&acc)[NS][1][4]) {
+    constexpr int UB = kUnitBytes * NS;
+    const int g = lane >> 2;
+    const uint4 v0 = *reinterpret_cast<const uint4*>(xs + cj * 1024 + lane * 16);
+    const uint4 v1 = *reinterpret_cast<const uint4*>(xs + cj * 1024 + 512 + lane * 16);
+    const uint32_t b[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    const uint8_t* unit = stage + (j * kBlockTiles + warp) * UB;
+#pragma unroll
+    for (int si = 0; si < NS; ++si) {
+        const uint4 cw = *reinterpret_cast<const uint4*>(unit + si * kUnitBytes + lane * 16);
+        const uint2 sw =
+            *reinterpret_cast<const uint2*>(unit + si * kUnitBytes + kUnitCodeBytes + g * 8);
+        const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
+        float d[4];
+#pragma unroll
+        for (int jb = 0; jb < 4; ++jb) {
+            uint32_t a0, a1, a2, a3;
+            e2m1x8_to_f16x2x4(cws[jb], a0, a1, a2, a3);
+            if (jb == 0)
+                mma_f16_16816_zero(d, a0, a1, a2, a3, b[0], b[1]);
+            else
+                mma_f16_16816(d, a0, a1, a2, a3, b[2 * jb], b[2 * jb + 1]);
+        }
+        // bytes 2t, 2t+1 of the row pair's 8 scale bytes: block t of rows g, g+8
+        const uint32_t s2 = e4m3x2_to_f16x2(prmt(sw.x, sw.y, scale_sel));
+        const float sgf = __half2float(__ushort_as_half((unsigned short)(s2 & 0xFFFFu)));
+        const float sg8f = __half2float(__ushort_as_half((unsigned short)(s2 >> 16)));
+        acc[si][0][0] = fmaf(d[0], sgf, acc[si][0][0]);
+        acc[si][0][2] = fmaf(d[2], sg8f, acc[si][0][2]);
+        if (!ONE) {
+            acc[si][0][1] = fmaf(d[1], sgf, acc[si][0][1]);
+            acc[si][0][3] = fmaf(d[3], sg8f, acc[si][0][3]);
         }
     }
 }
@@ -571,7 +703,8 @@ __device__ __forceinline__ void issue_step(const KArgs& a, const StepCursor& cur
 }
 
 // ONE: a single token row (M == 1), which needs only the even MMA columns.
-template <int NS, int NT, bool ONE>
+// DIAG: M <= 2 with the diagonal token layout (stage_x_diag).
+template <int NS, int NT, bool ONE, bool DIAG>
 __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a) {
     constexpr int CPS = kUnitsPerStep / NS;  // chunks per step
 
@@ -587,6 +720,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tq = lane & 3;
+    // diagonal layout: PRMT selector of scale bytes 2tq, 2tq+1 (block tq)
+    const uint32_t scale_sel = (uint32_t)(2 * tq) | ((uint32_t)(2 * tq + 1) << 4);
+    (void)scale_sel;
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
             mbar_init(full0 + 8u * s, 1);
@@ -652,13 +788,17 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
         const int c_start = cur.cb * CPS;
         const int nx = (q1 - q0) * CPS < a.C ? (q1 - q0) * CPS : a.C;
         __syncthreads();  // every warp is done with the previous range's x
-        stage_x<NT>(a, xs, c_start, nx, tok_unscale, amax_u);
+        if (DIAG)
+            stage_x_diag(a, xs, c_start, nx, tok_unscale, amax_u);
+        else
+            stage_x<NT>(a, xs, c_start, nx, tok_unscale, amax_u);
         if (!filled) fill_ring();
         float unscale[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) unscale[nt][e] = tok_unscale[nt * 8 + 2 * tq + e];
+            for (int e = 0; e < 2; ++e)
+                unscale[nt][e] = tok_unscale[DIAG ? e : nt * 8 + 2 * tq + e];
         int ci = 0, folded = 0;
         while (cur.valid(a) && cur.r == r) {
             if (ok && !mbar_wait_bounded(full0 + 8u * st, ph, abort_flag)) {
@@ -669,9 +809,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
             if (ok) {
                 const uint8_t* stage = smem + (size_t)st * a.stage_bytes;
 #pragma unroll
-                for (int j = 0; j < CPS; ++j)
-                    process_chunk<NS, NT, ONE>(stage, xs, a.x_stride, a.M, j, ci + j, warp, lane,
-                                               acc);
+                for (int j = 0; j < CPS; ++j) {
+                    if constexpr (DIAG)
+                        process_chunk_diag<NS, ONE>(stage, xs, j, ci + j, warp, lane, scale_sel,
+                                                    acc);
+                    else
+                        process_chunk<NS, NT, ONE>(stage, xs, a.x_stride, a.M, j, ci + j, warp,
+                                                   lane, acc);
+                }
             }
             // Release the stage; the last warp out refills it a ring ahead.
             __syncwarp();
@@ -710,8 +855,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
                             acc[si][nt][e] = 0.0f;
                         }
             }
-            if (seg_end &&
-                finish_segment<NS, NT>(a, hi, lo, unscale, r, q0, rb_now, cb_now, warp, lane, ok)) {
+            if (seg_end && finish_segment<NS, NT, DIAG>(a, hi, lo, unscale, r, q0, rb_now, cb_now,
+                                                        warp, lane, ok)) {
                 if (n_pending < kMaxPending)
                     pending[n_pending++] = rb_now;
                 else
@@ -753,13 +898,13 @@ size_t gemv_scratch_bytes(int streams, int M, int N, int K, int num_sms) {
     return make_plan(streams, M, N, K, num_sms).total;
 }
 
-template <int NS, int NT, bool ONE>
+template <int NS, int NT, bool ONE, bool DIAG>
 static cudaError_t launch_t(const Plan& p, const KArgs& a, cudaStream_t s) {
     static bool attr_done[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(stream_gemv_kernel<NS, NT, ONE>,
+        cudaError_t e = cudaFuncSetAttribute(stream_gemv_kernel<NS, NT, ONE, DIAG>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
@@ -774,7 +919,7 @@ static cudaError_t launch_t(const Plan& p, const KArgs& a, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, stream_gemv_kernel<NS, NT, ONE>, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, stream_gemv_kernel<NS, NT, ONE, DIAG>, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -818,11 +963,14 @@ cudaError_t launch_stream_gemv(int streams, const void* x, int M, int K, const v
     a.div_L = FastDiv::make((unsigned)(p.L < (1LL << 32) ? p.L : 1));
     a.div_CS = FastDiv::make((unsigned)p.CS);
     if (streams == 1) {
-        if (M == 1) return launch_t<1, 1, true>(p, a, s);
-        return p.NT == 1 ? launch_t<1, 1, false>(p, a, s) : launch_t<1, 2, false>(p, a, s);
+        if (M == 1) return launch_t<1, 1, true, true>(p, a, s);
+        if (M == 2) return launch_t<1, 1, false, true>(p, a, s);
+        return p.NT == 1 ? launch_t<1, 1, false, false>(p, a, s)
+                         : launch_t<1, 2, false, false>(p, a, s);
     }
-    if (M == 1) return launch_t<2, 1, true>(p, a, s);
-    return p.NT == 1 ? launch_t<2, 1, false>(p, a, s) : launch_t<2, 2, false>(p, a, s);
+    if (M == 1) return launch_t<2, 1, true, true>(p, a, s);
+    if (M == 2) return launch_t<2, 1, false, true>(p, a, s);
+    return p.NT == 1 ? launch_t<2, 1, false, false>(p, a, s) : launch_t<2, 2, false, false>(p, a, s);
 }
 
 }  // namespace nvf
