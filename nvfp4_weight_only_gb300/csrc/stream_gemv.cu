@@ -278,68 +278,72 @@ __device__ __forceinline__ uint32_t scale_pair_to_f16(uint32_t pr, unsigned bias
 template <int NT>
 __device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float* tok_unscale,
                         unsigned* amax_u) {
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid < 16) amax_u[tid] = 0u;
     __syncthreads();
+    // Warps are dealt to tokens, wpt per token, so that every index below is
+    // a shift or an add and a token's amax is one warp reduction.
+    const int wpt = kWarps / a.M;
+    const int m = warp / wpt, wi = warp - m * wpt;
     const int per_token = nx * 8;  // 16-byte groups of 8 k per token
-    const int items = a.M * per_token;
+    const int stride = wpt * 32;
     float mx_local = 0.0f;
-    int m_local = -1;
-    // Each thread's items go in rounds of kLoads: all loads of a round are in
-    // flight together before any value is used.
-    constexpr int kLoads = 8;
-    for (int base = tid; base < items; base += kLoads * kThreads) {
-        uint4 v[kLoads];
+    if (m < a.M) {
+        const __nv_bfloat16* xrow = a.x + (size_t)m * a.K;
+        uint8_t* row = xs + m * a.x_stride;
+        // A lane's groups go in rounds of kLoads: all loads of a round are in
+        // flight together before any value is used.
+        constexpr int kLoads = 8;
+        for (int base = wi * 32 + lane; base < per_token; base += kLoads * stride) {
+            uint4 v[kLoads];
 #pragma unroll
-        for (int u = 0; u < kLoads; ++u) {
-            const int it = base + u * kThreads;
-            v[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (it < items) {
-                const int m = it / per_token, q = it - m * per_token;
-                int c = c_start + (q >> 3);
-                if (c >= a.C) c -= a.C;
-                const int k0 = c * kChunkK + (q & 7) * 8;
-                if (k0 < a.K) v[u] = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)m * a.K + k0));
+            for (int u = 0; u < kLoads; ++u) {
+                const int q = base + u * stride;
+                v[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (q < per_token) {
+                    int c = c_start + (q >> 3);
+                    if (c >= a.C) c -= a.C;
+                    const int k0 = c * kChunkK + (q & 7) * 8;
+                    if (k0 < a.K) v[u] = __ldg(reinterpret_cast<const uint4*>(xrow + k0));
+                }
             }
-        }
 #pragma unroll
-        for (int u = 0; u < kLoads; ++u) {
-            const int it = base + u * kThreads;
-            if (it >= items) break;
-            const int m = it / per_token, q = it - m * per_token;
-            const int ci = q >> 3, grp = q & 7;  // grp: k0 = 8*grp within the chunk
-            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-            float mx = 0.0f;
+            for (int u = 0; u < kLoads; ++u) {
+                const int q = base + u * stride;
+                if (q >= per_token) break;
+                const int ci = q >> 3, grp = q & 7;  // grp: k0 = 8*grp within the chunk
+                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                mx = fmaxf(mx, fabsf(__uint_as_float(w[i] << 16)));
-                mx = fmaxf(mx, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+                for (int i = 0; i < 4; ++i) {
+                    mx_local = fmaxf(mx_local, fabsf(__uint_as_float(w[i] << 16)));
+                    mx_local = fmaxf(mx_local, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+                }
+                // pair i (k = k0 + 2i, +1) belongs to lane quarter t = i, block
+                // j = grp/2, half = grp&1 (b0 for k%16 < 8, b1 otherwise)
+                uint8_t* dst = row + ci * 128 + (grp >> 1) * 8 + (grp & 1) * 4;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) *reinterpret_cast<uint32_t*>(dst + i * 32) = w[i];
             }
-            // pair i (k = k0 + 2i, +1) belongs to lane quarter t = i, block j =
-            // grp/2, half = grp&1 (b0 for k%16 < 8, b1 otherwise)
-            uint8_t* dst = xs + m * a.x_stride + ci * 128 + (grp >> 1) * 8 + (grp & 1) * 4;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) *reinterpret_cast<uint32_t*>(dst + i * 32) = w[i];
-            if (m != m_local) {
-                if (m_local >= 0 && mx_local > 0.0f)
-                    atomicMax(&amax_u[m_local], __float_as_uint(mx_local));
-                m_local = m;
-                mx_local = 0.0f;
-            }
-            mx_local = fmaxf(mx_local, mx);
         }
     }
-    if (m_local >= 0 && mx_local > 0.0f) atomicMax(&amax_u[m_local], __float_as_uint(mx_local));
+    // amax >= 0, so its bit pattern orders like its value
+    const unsigned wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(mx_local));
+    if (lane == 0 && m < a.M && wmax != 0u) atomicMax(&amax_u[m], wmax);
     __syncthreads();
     token_scales(amax_u, tok_unscale);
     __syncthreads();
-    const int words = a.M * nx * 32;  // 32-bit words (bf16 pairs) to convert
-    for (int it = tid; it < words; it += kThreads) {
-        const int m = it / (nx * 32), wi = it - m * (nx * 32);
-        uint32_t* p = reinterpret_cast<uint32_t*>(xs + m * a.x_stride) + wi;
-        *p = scale_pair_to_f16(*p, amax_u[m]);
+    if (m < a.M) {  // exact power-of-two f16 conversion, 16 bytes per lane
+        uint4* row = reinterpret_cast<uint4*>(xs + m * a.x_stride);
+        const unsigned biased = amax_u[m];
+        for (int i = wi * 32 + lane; i < nx * 8; i += stride) {
+            uint4 w = row[i];
+            w.x = scale_pair_to_f16(w.x, biased);
+            w.y = scale_pair_to_f16(w.y, biased);
+            w.z = scale_pair_to_f16(w.z, biased);
+            w.w = scale_pair_to_f16(w.w, biased);
+            row[i] = w;
+        }
     }
-    (void)lane;
     __syncthreads();
 }
 
@@ -355,17 +359,17 @@ __device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float*
 // power-of-two f16 conversion), after a zero fill of the chunks.
 __device__ void stage_x_diag(const KArgs& a, uint8_t* xs, int c_start, int nx, float* tok_unscale,
                              unsigned* amax_u) {
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid < 16) amax_u[tid] = 0u;
     for (int i = tid; i < nx * 64; i += kThreads)
         reinterpret_cast<uint4*>(xs)[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
+    const int wpt = kWarps / a.M;  // warps per token (M <= 2)
+    const int m = warp / wpt, wi = warp - m * wpt;
     const int per_token = nx * 8;  // 16-byte groups of 8 k per token
-    const int items = a.M * per_token;
+    const int stride = wpt * 32;
     float mx_local = 0.0f;
-    int m_local = -1;
-    for (int it = tid; it < items; it += kThreads) {
-        const int m = it / per_token, q = it - m * per_token;
+    for (int q = wi * 32 + lane; q < per_token; q += stride) {
         const int ci = q >> 3, grp = q & 7;  // k0 = 8*grp within the chunk
         int c = c_start + ci;
         if (c >= a.C) c -= a.C;
@@ -373,38 +377,33 @@ __device__ void stage_x_diag(const KArgs& a, uint8_t* xs, int c_start, int nx, f
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (k0 < a.K) v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)m * a.K + k0));
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        float mx = 0.0f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            mx = fmaxf(mx, fabsf(__uint_as_float(w[i] << 16)));
-            mx = fmaxf(mx, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+            mx_local = fmaxf(mx_local, fabsf(__uint_as_float(w[i] << 16)));
+            mx_local = fmaxf(mx_local, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
         }
         // pair i (k = 8*grp + 2i): block j = grp/2, half b = grp&1, quarter t = i
         const int j = grp >> 1, b = grp & 1;
         uint8_t* dst = xs + ci * 1024 + (j >> 1) * 512 + (4 * (2 * j + m)) * 16 + 4 * (2 * (j & 1) + b);
 #pragma unroll
         for (int i = 0; i < 4; ++i) *reinterpret_cast<uint32_t*>(dst + 16 * i) = w[i];
-        if (m != m_local) {
-            if (m_local >= 0 && mx_local > 0.0f)
-                atomicMax(&amax_u[m_local], __float_as_uint(mx_local));
-            m_local = m;
-            mx_local = 0.0f;
-        }
-        mx_local = fmaxf(mx_local, mx);
     }
-    if (m_local >= 0 && mx_local > 0.0f) atomicMax(&amax_u[m_local], __float_as_uint(mx_local));
+    const unsigned wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(mx_local));
+    if (lane == 0 && wmax != 0u) atomicMax(&amax_u[m], wmax);
     __syncthreads();
     token_scales(amax_u, tok_unscale);
     __syncthreads();
-    // convert the M*32 non-zero words of every chunk: (m, j, t, b)
-    const int words = nx * a.M * 32;
-    for (int it = tid; it < words; it += kThreads) {
-        const int ci = it / (a.M * 32), rem = it - ci * (a.M * 32);
-        const int m = rem >> 5, w5 = rem & 31;
-        const int j = w5 >> 3, t = (w5 >> 1) & 3, b = w5 & 1;
-        uint32_t* p = reinterpret_cast<uint32_t*>(xs + ci * 1024 + (j >> 1) * 512 +
-                                                  (4 * (2 * j + m) + t) * 16 + 4 * (2 * (j & 1) + b));
-        *p = scale_pair_to_f16(*p, amax_u[m]);
+    // convert the token's non-zero words: per chunk, block j and quarter t, the
+    // two words (b = 0, 1) at lane 4(2j + m) + t
+    const unsigned biased = amax_u[m];
+    for (int it = wi * 32 + lane; it < nx * 16; it += stride) {
+        const int ci = it >> 4, j = (it >> 2) & 3, t = it & 3;
+        uint2* p = reinterpret_cast<uint2*>(xs + ci * 1024 + (j >> 1) * 512 +
+                                            (4 * (2 * j + m) + t) * 16 + 8 * (j & 1));
+        uint2 w = *p;
+        w.x = scale_pair_to_f16(w.x, biased);
+        w.y = scale_pair_to_f16(w.y, biased);
+        *p = w;
     }
     __syncthreads();
 }
