@@ -47,19 +47,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same test, allowing the hardware to suspend the thread until the phase
+// completes or hint_ns have passed, so waiting warps do not spin on the
+// issue slots the working warps need.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Longest single suspension inside a bounded wait; the abort flag and the
+// time limit are checked between suspensions.
+constexpr uint32_t kSuspendHintNs = 20000;
+
 // Waits for the phase with the given parity to complete.  Gives up (returns
-// false) after kWaitLimitNs, or at once when *abort is set by another warp.
+// false) after kWaitLimitNs, or when *abort is set by another warp (noticed
+// within one suspension).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   const volatile int* abort) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
     const unsigned long long t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 15u) == 0) {
-            if (*abort) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-        }
+    for (;;) {
+        if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
 }
 
