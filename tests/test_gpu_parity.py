@@ -152,9 +152,29 @@ def test_gemv_deterministic_and_reusable_workspace(dev):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("N,K,M", [(5120, 17408, 1), (5120, 17408, 8), (17408, 5120, 16),
-                                   (4096, 21504, 1)])
+                                   (4096, 21504, 1), (65536, 4096, 16), (21504, 5376, 3)])
 def test_gemv_full_size(dev, N, K, M):
     run_gemv_case(dev, N, K, M, seed=11, outliers=0.01 if M > 1 else 0.0)
+
+
+@pytest.mark.slow
+def test_gemv_largest_sweep_shape_sampled_rows(dev):
+    """N=65536, K=21504 (the top of the standalone GEMV sweep), M=2: the oracle
+    quantises the whole weight, the GPU runs the GEMV on those codes, and 640
+    rows (both ends and a seeded sample) are checked against the oracle's GEMV
+    of just those rows."""
+    N, K, M = 65536, 21504, 2
+    w = synth.weights_f32(N, K, seed=77)
+    rc, rs, rs2 = oracle.quantize(w.numpy())
+    del w
+    p = ffi.nvfp4_repack(torch.from_numpy(rc).to(dev), torch.from_numpy(rs).to(dev), N, K)
+    x = synth.activations_bf16(M, K, seed=5, outlier_frac=0.01)
+    y = ffi.nvfp4_gemv(x.to(dev), p, float(rs2), N)
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([np.arange(64), np.arange(N - 64, N),
+                                     rng.choice(N, 512, replace=False)]))
+    ref = oracle.gemv(synth.bf16_bits(x), rc[rows], rs[rows], rs2, len(rows))
+    assert_close(y[:, torch.from_numpy(rows).to(dev)], ref, "gemv 65536x21504 sampled rows")
 
 
 # ------------------------------------------------------------------ FFN
@@ -319,6 +339,14 @@ def test_ffn_zero_gate_and_zero_input(dev):
                                             (16, ffi.NVFP4_ACT_SILU, 0.01)])
 def test_ffn_full_size(dev, M, act, outliers):
     run_ffn_case(dev, 5120, 17408, M, act, outliers=outliers, seed=M)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("M,act", [(1, ffi.NVFP4_ACT_SILU), (5, ffi.NVFP4_ACT_GELU_TANH),
+                                   (12, ffi.NVFP4_ACT_SILU)])
+def test_ffn_large_dense_shape(dev, M, act):
+    """The large dense FFN sweep's layer shape, H=5376, I=21504."""
+    run_ffn_case(dev, 5376, 21504, M, act, outliers=0.0, seed=100 + M)
 
 
 def test_error_codes_raise(dev):
