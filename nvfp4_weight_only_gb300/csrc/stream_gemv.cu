@@ -419,23 +419,32 @@ __device__ __forceinline__ float* tile_slot(const KArgs& a, int r, int rb, int w
     return a.partials + ((size_t)r * a.s_max + si_slot) * slot + (size_t)warp * NS * kTileRows * a.M;
 }
 
-// Count this warp's partial of (row block rb, tile) as arrived; true when it
-// was the last of the ranges covering rb, which then reduces the tile.  The
-// caller has fenced its slot stores (GPU scope) before calling.
-__device__ __forceinline__ bool publish_tile(const KArgs& a, int rb, int warp, int lane) {
+// Count this warp's partial of (row block rb, tile) as arrived.  The
+// increment is acquire-release at GPU scope: the slot stores of every lane,
+// ordered before it by the caller's __syncwarp, are visible to the range that
+// observes the final count, and that range sees the others' slots.  The warp
+// does not wait for the returned count here: a segment that closes in the
+// middle of a range keeps streaming, and the count is examined after the
+// range's last step (resolve_tile).
+__device__ __forceinline__ int publish_tile(const KArgs& a, int rb, int warp, int lane) {
+    int old = 0;
+    if (lane == 0) old = atom_add_acq_rel_gpu(a.counters + rb * kBlockTiles + warp, 1);
+    return old;  // lane 0 only; consumed later by resolve_tile
+}
+
+// Whether the publication that returned `old` (lane 0) was the last of the
+// ranges covering rb; the last one resets the counter for the next call.
+__device__ __forceinline__ bool resolve_tile(const KArgs& a, int rb, int warp, int lane, int old) {
     int last = 0;
     if (lane == 0) {
         const long long p_lo = (long long)rb * a.CS;
         const int nparts = range_of(a, p_lo + a.CS - 1) - range_of(a, p_lo) + 1;
-        int* cnt = a.counters + rb * kBlockTiles + warp;
-        const int old = atomicAdd(cnt, 1);
         last = (old == nparts - 1) ? 1 : 0;
-        if (last) {
-            *cnt = 0;  // ready for the next call
-            __threadfence();
-        }
+        if (last) a.counters[rb * kBlockTiles + warp] = 0;  // ready for the next call
     }
-    return __shfl_sync(0xffffffffu, last, 0) != 0;
+    last = __shfl_sync(0xffffffffu, last, 0);
+    __syncwarp();  // the other lanes' slot loads follow lane 0's acquire
+    return last != 0;
 }
 
 // End of the segment of row block rb (last step cb_last) that range r covers,
@@ -445,7 +454,7 @@ __device__ __forceinline__ bool publish_tile(const KArgs& a, int rb, int warp, i
 // function returns true when this range arrived last for the tile and must
 // reduce it (done after the stream, by reduce_tile).
 template <int NS, int NT, bool DIAG>
-__device__ __forceinline__ bool finish_segment(const KArgs& a, float (&hi)[NS][NT][4],
+__device__ __forceinline__ int finish_segment(const KArgs& a, float (&hi)[NS][NT][4],
                                                float (&lo)[NS][NT][4],
                                                const float (&unscale)[NT][2], int r, int q0,
                                                int rb, int cb_last, int warp, int lane, bool ok) {
@@ -481,7 +490,7 @@ __device__ __forceinline__ bool finish_segment(const KArgs& a, float (&hi)[NS][N
                 if (ok && lane_stores && row < a.N && token < a.M)
                     store_output<NS>(a, row, token, v[0][nt][e], v[NS - 1][nt][e]);
             }
-        return false;
+        return -1;
     }
     float* slot = tile_slot<NS>(a, r, rb, warp);
 #pragma unroll
@@ -494,7 +503,6 @@ __device__ __forceinline__ bool finish_segment(const KArgs& a, float (&hi)[NS][N
                 if (lane_stores && token < a.M)
                     slot[(si * kTileRows + g + 8 * (e >> 1)) * a.M + token] = v[si][nt][e];
             }
-    __threadfence();
     __syncwarp();
     return publish_tile(a, rb, warp, lane);
 }
@@ -779,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
     bool ok = true;
     // row blocks whose tile this warp must still reduce (it arrived last)
     constexpr int kMaxPending = 4;
-    int pending[kMaxPending];
+    int pending[kMaxPending], pending_old[kMaxPending];
     int n_pending = 0;
     while (cur.valid(a)) {
         // ---- a new range: stage its token rows
@@ -854,16 +862,29 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
                             acc[si][nt][e] = 0.0f;
                         }
             }
-            if (seg_end && finish_segment<NS, NT, DIAG>(a, hi, lo, unscale, r, q0, rb_now, cb_now,
-                                                        warp, lane, ok)) {
-                if (n_pending < kMaxPending)
-                    pending[n_pending++] = rb_now;
-                else
-                    reduce_tile<NS, NT>(a, rb_now, warp, lane, ok);
+            if (seg_end) {
+                const int old = finish_segment<NS, NT, DIAG>(a, hi, lo, unscale, r, q0, rb_now,
+                                                             cb_now, warp, lane, ok);
+                if (old >= 0) {
+                    if (n_pending == kMaxPending) {  // resolve the oldest now
+                        if (resolve_tile(a, pending[0], warp, lane, pending_old[0]))
+                            reduce_tile<NS, NT>(a, pending[0], warp, lane, ok);
+                        for (int i = 1; i < kMaxPending; ++i) {
+                            pending[i - 1] = pending[i];
+                            pending_old[i - 1] = pending_old[i];
+                        }
+                        --n_pending;
+                    }
+                    pending[n_pending] = rb_now;
+                    pending_old[n_pending] = old;
+                    ++n_pending;
+                }
             }
         }
     }
-    for (int i = 0; i < n_pending; ++i) reduce_tile<NS, NT>(a, pending[i], warp, lane, ok);
+    for (int i = 0; i < n_pending; ++i)
+        if (resolve_tile(a, pending[i], warp, lane, pending_old[i]))
+            reduce_tile<NS, NT>(a, pending[i], warp, lane, ok);
     // A CTA that abandoned a wait still owns copies in flight: wait for them
     // (bounded) before the shared memory is released.
     __syncthreads();
