@@ -35,13 +35,22 @@
 
 namespace nvf {
 
-constexpr int kWarps = kBlockTiles;  // one warp per 16-row tile of a row block
-constexpr int kThreads = kWarps * 32;
+constexpr int kWarps = kBlockTiles;  // consumer warps: one per 16-row tile of a row block
+constexpr int kConsumerThreads = kWarps * 32;
+// + one producer warpgroup, whose first lane issues every bulk copy.  The
+// register file is re-split at entry (setmaxnreg): launched at 96 per thread
+// (640 x 96 = 61440), the producer warpgroup drops to 24 and the consumers
+// rise to 112 (512 x 112 + 128 x 24 = 60416 <= 61440).
+constexpr int kThreads = kConsumerThreads + 128;
+constexpr int kLaunchRegs = 96, kProducerRegs = 24, kConsumerRegs = 112;
+static_assert(kConsumerThreads * kConsumerRegs + 128 * kProducerRegs <= kThreads * kLaunchRegs,
+              "setmaxnreg split exceeds the launch allocation");
 constexpr int kSmemMax = 227 * 1024;
 constexpr int kXBudget = 96 * 1024;
 constexpr int kRingBudget = 200 * 1024;
 constexpr int kMaxStages = 8;
 constexpr int kMiscBytes = 512;
+constexpr int kMiscIssuesOff = 256;  // per-stage copy counts (kMaxStages ints) in the misc area
 // Chunks (of 64 K elements) summed in plain fp32 before the sum is folded into
 // the exact hi/lo pair.
 constexpr int kFoldChunks = 8;
@@ -240,6 +249,9 @@ __device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float b) {
     lo += err;
 }
 
+// Barrier over the consumer warps only (the producer warp never joins).
+__device__ __forceinline__ void consumer_sync() { named_barrier_sync(1, kConsumerThreads); }
+
 // Per token m (threads 0..15): the exponent e_m with amax_m * 2^e_m in
 // [2^14, 2^15), kept biased in amax_u[m] for the conversion pass, and the
 // unscale factor 2^-e_m for the fp32 results.
@@ -280,7 +292,7 @@ __device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float*
                         unsigned* amax_u) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid < 16) amax_u[tid] = 0u;
-    __syncthreads();
+    consumer_sync();
     // Warps are dealt to tokens, wpt per token, so that every index below is
     // a shift or an add and a token's amax is one warp reduction.
     const int wpt = kWarps / a.M;
@@ -329,9 +341,9 @@ __device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float*
     // amax >= 0, so its bit pattern orders like its value
     const unsigned wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(mx_local));
     if (lane == 0 && m < a.M && wmax != 0u) atomicMax(&amax_u[m], wmax);
-    __syncthreads();
+    consumer_sync();
     token_scales(amax_u, tok_unscale);
-    __syncthreads();
+    consumer_sync();
     if (m < a.M) {  // exact power-of-two f16 conversion, 16 bytes per lane
         uint4* row = reinterpret_cast<uint4*>(xs + m * a.x_stride);
         const unsigned biased = amax_u[m];
@@ -344,7 +356,7 @@ __device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float*
             row[i] = w;
         }
     }
-    __syncthreads();
+    consumer_sync();
 }
 
 // Token rows for one or two tokens ("diagonal" B operand).  The 8 columns of
@@ -361,9 +373,9 @@ __device__ void stage_x_diag(const KArgs& a, uint8_t* xs, int c_start, int nx, f
                              unsigned* amax_u) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid < 16) amax_u[tid] = 0u;
-    for (int i = tid; i < nx * 64; i += kThreads)
+    for (int i = tid; i < nx * 64; i += kConsumerThreads)
         reinterpret_cast<uint4*>(xs)[i] = make_uint4(0u, 0u, 0u, 0u);
-    __syncthreads();
+    consumer_sync();
     const int wpt = kWarps / a.M;  // warps per token (M <= 2)
     const int m = warp / wpt, wi = warp - m * wpt;
     const int per_token = nx * 8;  // 16-byte groups of 8 k per token
@@ -390,9 +402,9 @@ __device__ void stage_x_diag(const KArgs& a, uint8_t* xs, int c_start, int nx, f
     }
     const unsigned wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(mx_local));
     if (lane == 0 && wmax != 0u) atomicMax(&amax_u[m], wmax);
-    __syncthreads();
+    consumer_sync();
     token_scales(amax_u, tok_unscale);
-    __syncthreads();
+    consumer_sync();
     // convert the token's non-zero words: per chunk, block j and quarter t, the
     // two words (b = 0, 1) at lane 4(2j + m) + t
     const unsigned biased = amax_u[m];
@@ -405,7 +417,7 @@ __device__ void stage_x_diag(const KArgs& a, uint8_t* xs, int c_start, int nx, f
         w.y = scale_pair_to_f16(w.y, biased);
         *p = w;
     }
-    __syncthreads();
+    consumer_sync();
 }
 
 // Split-K bookkeeping of one warp's tile.  Slot (range r, segment index) holds,
@@ -718,12 +730,12 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t ring_s = smem_addr(smem);
     uint8_t* xs = smem + a.x_off;
-    const uint32_t full0 = smem_addr(smem + a.bar_off);
-    int* done = reinterpret_cast<int*>(smem + a.cnt_off);  // warps finished with a stage
-    int* issues = done + a.stages;                          // copies issued into a stage
+    const uint32_t full0 = smem_addr(smem + a.bar_off);   // stage filled (tx bytes)
+    const uint32_t empty0 = smem_addr(smem + a.cnt_off);  // stage released by all consumers
     float* tok_unscale = reinterpret_cast<float*>(smem + a.misc_off);
     unsigned* amax_u = reinterpret_cast<unsigned*>(tok_unscale + 16);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(amax_u + 16);
+    int* issues = reinterpret_cast<int*>(smem + a.misc_off + kMiscIssuesOff);  // copies per stage
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tq = lane & 3;
@@ -733,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
             mbar_init(full0 + 8u * s, 1);
-            done[s] = 0;
+            mbar_init(empty0 + 8u * s, kWarps);
             issues[s] = 0;
         }
         *abort_flag = 0;
@@ -743,33 +755,48 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
     // Let the next kernel on the stream launch as SMs free up; it will wait
     // for this grid before it touches anything this grid writes.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // Weights are never written by the preceding kernel when early_weights is
-    // set (the down projection after the dual kernel), so the ring can start
-    // filling before the wait; otherwise the wait comes first.
-    if (!a.early_weights) asm volatile("griddepcontrol.wait;" ::: "memory");
-    // Initial fill of the ring; afterwards `ahead` (kept by every warp) points
-    // at the step one full ring ahead of the step being consumed.  Without
-    // early_weights the fill waits until the first range's token rows are in
-    // shared memory, so those few loads are not queued behind the burst.
-    StepCursor cur, ahead;
-    cur.init(a);
-    ahead.init(a);
-    bool filled = false;
-    auto fill_ring = [&]() {
-        if (threadIdx.x == 0) {
-            for (int st = 0; st < a.stages && ahead.valid(a); ++st) {
-                issue_step<NS>(a, ahead, st, ring_s, full0, issues);
+
+    if (warp >= kWarps) {
+        // ---- producer warpgroup: lane 0 of its first warp streams every step
+        // of this CTA's ranges through the ring.  Weights are never written by
+        // the preceding kernel when early_weights is set, so the ring fills
+        // before the wait on it.
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
+        if (warp == kWarps && lane == 0) {
+            if (!a.early_weights) asm volatile("griddepcontrol.wait;" ::: "memory");
+            StepCursor ahead;
+            ahead.init(a);
+            int pst = 0, round = 0;
+            while (ahead.valid(a) && !*abort_flag) {
+                // refilling a stage: wait until all consumer warps released it
+                if (round > 0 && !mbar_wait_bounded(empty0 + 8u * pst,
+                                                    (uint32_t)((round - 1) & 1), abort_flag)) {
+                    *abort_flag = 1;
+                    atomicOr(a.status, 1);
+                    break;
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue_step<NS>(a, ahead, pst, ring_s, full0, issues);
                 ahead.advance(a);
+                if (++pst == a.stages) {
+                    pst = 0;
+                    ++round;
+                }
             }
-        } else {
-            for (int st = 0; st < a.stages && ahead.valid(a); ++st) ahead.advance(a);
+            // Every copy must have landed before the CTA (and its shared
+            // memory) goes away; the consumers wait for all of them unless a
+            // wait was abandoned, so this only waits in that case.
+            const int zero = 0;
+            for (int s = 0; s < a.stages; ++s)
+                if (issues[s] > 0)
+                    mbar_wait_bounded(full0 + 8u * s, (uint32_t)((issues[s] - 1) & 1), &zero);
         }
-        filled = true;
-    };
-    if (a.early_weights) {
-        fill_ring();
-        asm volatile("griddepcontrol.wait;" ::: "memory");
+        return;
     }
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    StepCursor cur;
+    cur.init(a);
 
     float acc[NS][NT][4], hi[NS][NT][4], lo[NS][NT][4];
 #pragma unroll
@@ -794,12 +821,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
         const int r = cur.r, q0 = cur.q, q1 = cur.q_end;
         const int c_start = cur.cb * CPS;
         const int nx = (q1 - q0) * CPS < a.C ? (q1 - q0) * CPS : a.C;
-        __syncthreads();  // every warp is done with the previous range's x
+        consumer_sync();  // every warp is done with the previous range's x
         if (DIAG)
             stage_x_diag(a, xs, c_start, nx, tok_unscale, amax_u);
         else
             stage_x<NT>(a, xs, c_start, nx, tok_unscale, amax_u);
-        if (!filled) fill_ring();
         float unscale[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -825,21 +851,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
                                                    lane, acc);
                 }
             }
-            // Release the stage; the last warp out refills it a ring ahead.
+            // Release the stage to the producer.
             __syncwarp();
-            if (lane == 0) {
-                __threadfence_block();
-                const int old = atomicAdd(&done[st], 1);
-                if (old == kWarps - 1) {
-                    done[st] = 0;
-                    __threadfence_block();
-                    if (ahead.valid(a) && !*abort_flag) {
-                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                        issue_step<NS>(a, ahead, st, ring_s, full0, issues);
-                    }
-                }
-            }
-            ahead.advance(a);
+            if (lane == 0) mbar_arrive(empty0 + 8u * st);
             if (++st == a.stages) {
                 st = 0;
                 ph ^= 1u;
@@ -885,15 +899,6 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
     for (int i = 0; i < n_pending; ++i)
         if (resolve_tile(a, pending[i], warp, lane, pending_old[i]))
             reduce_tile<NS, NT>(a, pending[i], warp, lane, ok);
-    // A CTA that abandoned a wait still owns copies in flight: wait for them
-    // (bounded) before the shared memory is released.
-    __syncthreads();
-    if (*abort_flag && threadIdx.x == 0) {
-        const int zero = 0;
-        for (int s = 0; s < a.stages; ++s)
-            if (issues[s] > 0)
-                mbar_wait_bounded(full0 + 8u * s, (uint32_t)((issues[s] - 1) & 1), &zero);
-    }
 }
 
 int device_sm_count() {
