@@ -150,6 +150,28 @@ def test_gemv_deterministic_and_reusable_workspace(dev):
     assert ffi.nvfp4_workspace_status(ws) == 0
 
 
+@pytest.mark.parametrize("M", [2, 5, 12])
+def test_gemv_token_rows_are_independent(dev, M):
+    """Permuting the token rows permutes the outputs bit for bit (each row is
+    scaled and accumulated on its own), and the FFN on a permutation of x is
+    the same permutation of its output."""
+    N, K = 1024, 2048
+    w = synth.weights_f32(N, K, seed=31)
+    c, s, s2 = gpu_quant(w, dev)
+    p = ffi.nvfp4_repack(c, s, N, K)
+    x = synth.activations_bf16(M, K, seed=32, outlier_frac=0.05).to(dev)
+    perm = torch.from_numpy(np.random.default_rng(M).permutation(M)).to(dev)
+    y = ffi.nvfp4_gemv(x, p, s2, N)
+    yp = ffi.nvfp4_gemv(x[perm].contiguous(), p, s2, N)
+    assert torch.equal(yp, y[perm])
+    H, I = 256, 512
+    gu, dn, q, _ = build_ffn(dev, H, I)
+    xf = synth.activations_bf16(M, H, seed=33, outlier_frac=0.05).to(dev)
+    o = ffi.ffn_swiglu_nvfp4(xf, gu, q[0][2], q[1][2], dn, q[2][2], I)
+    op = ffi.ffn_swiglu_nvfp4(xf[perm].contiguous(), gu, q[0][2], q[1][2], dn, q[2][2], I)
+    assert torch.equal(op, o[perm])
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("N,K,M", [(5120, 17408, 1), (5120, 17408, 8), (17408, 5120, 16),
                                    (4096, 21504, 1), (65536, 4096, 16), (21504, 5376, 3)])
