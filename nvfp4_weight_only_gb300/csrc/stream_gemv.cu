@@ -67,6 +67,7 @@ struct Plan {
     int grid, R;
     long long Pmax;         // steps per range (max)
     int cps, xcap, x_stride, stage_bytes, stages, s_max, slot_floats;
+    int part_stride;  // diagonal layout: parts per element, padded to 4 (0 otherwise)
     int x_off, bar_off, cnt_off, misc_off;
     size_t smem;
     size_t counters_off, partials_off, total;
@@ -118,7 +119,22 @@ static Plan make_plan(int NS, int M, int N, int K, int num_sms) {
     p.slot_floats = kBlockTiles * NS * kTileRows * M;
     p.counters_off = 0;
     p.partials_off = (size_t)ceil_div((long long)p.RB * kBlockTiles * 4, 256) * 256;
-    p.total = p.partials_off + (size_t)p.R * p.s_max * p.slot_floats * sizeof(float);
+    p.part_stride = 0;
+    if (diag) {
+        // element-major: the parts of one output element are contiguous, so the
+        // last range to arrive reads them with a few 16-byte loads
+        long long most = 1;
+        for (long long rb = 0; rb < p.RB; ++rb) {
+            const long long lo = rb * p.CS, hi = lo + p.CS - 1;
+            const long long parts = ((hi + 1) * p.R - 1) / p.L - ((lo + 1) * p.R - 1) / p.L + 1;
+            if (parts > most) most = parts;
+        }
+        p.part_stride = (int)ceil_div(most, 4) * 4;
+        p.total = p.partials_off +
+                  (size_t)p.RB * p.slot_floats * (size_t)p.part_stride * sizeof(float);
+    } else {
+        p.total = p.partials_off + (size_t)p.R * p.s_max * p.slot_floats * sizeof(float);
+    }
     return p;
 }
 
@@ -150,6 +166,7 @@ struct KArgs {
     long long L;
     int M, K, N, C, CS, RB, R, grid;
     int stages, stage_bytes, x_off, x_stride, bar_off, cnt_off, misc_off, s_max;
+    int part_stride;  // diagonal layout's element-major partials (parts per element)
     float scale_a, scale_b;
     int act;
     int early_weights;  // stream weights before waiting on the preceding kernel
@@ -504,17 +521,33 @@ __device__ __forceinline__ int finish_segment(const KArgs& a, float (&hi)[NS][NT
             }
         return -1;
     }
-    float* slot = tile_slot<NS>(a, r, rb, warp);
+    if (DIAG) {
+        // element-major: element (si, row, token) of the tile, part r - r_first
+        float* base = a.partials + (size_t)(rb * kBlockTiles + warp) * (NS * kTileRows * a.M) *
+                                       a.part_stride +
+                      (r - range_of(a, (long long)rb * a.CS));
 #pragma unroll
-    for (int si = 0; si < NS; ++si)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int si = 0; si < NS; ++si)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int token = DIAG ? (e & 1) : nt * 8 + 2 * tq + (e & 1);
+                const int token = e & 1;
                 if (lane_stores && token < a.M)
-                    slot[(si * kTileRows + g + 8 * (e >> 1)) * a.M + token] = v[si][nt][e];
+                    base[(size_t)((si * kTileRows + g + 8 * (e >> 1)) * a.M + token) *
+                         a.part_stride] = v[si][0][e];
             }
+    } else {
+        float* slot = tile_slot<NS>(a, r, rb, warp);
+#pragma unroll
+        for (int si = 0; si < NS; ++si)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int token = nt * 8 + 2 * tq + (e & 1);
+                    if (lane_stores && token < a.M)
+                        slot[(si * kTileRows + g + 8 * (e >> 1)) * a.M + token] = v[si][nt][e];
+                }
+    }
     __syncwarp();
     return publish_tile(a, rb, warp, lane);
 }
@@ -572,6 +605,56 @@ __device__ __forceinline__ void reduce_tile(const KArgs& a, int rb, int warp, in
 // than chained MMAs on GB300).  With two token tiles: folded into the A
 // fragments by an exact f16 multiply, so the MMAs accumulate directly and the
 // scaling is shared by both tiles.
+// reduce_tile for the diagonal layout's element-major partials: lane e owns
+// element e (< 16*M <= 32) of each stream and reads its parts in 16-byte
+// vectors, 16 parts per batch, summing them in range order.
+template <int NS>
+__device__ __forceinline__ void reduce_tile_diag(const KArgs& a, int rb, int warp, int lane,
+                                                 bool ok) {
+    const long long p_lo = (long long)rb * a.CS;
+    const int nparts = range_of(a, p_lo + a.CS - 1) - range_of(a, p_lo) + 1;
+    const int n_el = kTileRows * a.M;
+    const int e = lane;
+    if (e >= n_el) return;
+    const float* base = a.partials + (size_t)(rb * kBlockTiles + warp) * (NS * n_el) * a.part_stride;
+    float sum[NS];
+#pragma unroll
+    for (int si = 0; si < NS; ++si) sum[si] = 0.0f;
+    for (int p0 = 0; p0 < nparts; p0 += 16) {
+        float part[NS][16];
+#pragma unroll
+        for (int si = 0; si < NS; ++si) {
+            const float4* src = reinterpret_cast<const float4*>(
+                base + (size_t)(si * n_el + e) * a.part_stride + p0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 v4 = p0 + 4 * q < nparts ? __ldcg(src + q)
+                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                part[si][4 * q] = v4.x;
+                part[si][4 * q + 1] = v4.y;
+                part[si][4 * q + 2] = v4.z;
+                part[si][4 * q + 3] = v4.w;
+            }
+        }
+#pragma unroll
+        for (int si = 0; si < NS; ++si)
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                if (p0 + q < nparts) sum[si] += part[si][q];
+    }
+    const int token = e % a.M, row16 = e / a.M;
+    const int row = rb * kBlockRows + warp * kTileRows + row16;
+    if (ok && row < a.N) store_output<NS>(a, row, token, sum[0], sum[NS - 1]);
+}
+
+template <int NS, int NT, bool DIAG>
+__device__ __forceinline__ void reduce_any(const KArgs& a, int rb, int warp, int lane, bool ok) {
+    if constexpr (DIAG)
+        reduce_tile_diag<NS>(a, rb, warp, lane, ok);
+    else
+        reduce_tile<NS, NT>(a, rb, warp, lane, ok);
+}
+
 template <int NT>
 __device__ __forceinline__ constexpr bool kScaleInA() {
     return NT == 2;
@@ -882,7 +965,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
                 if (old >= 0) {
                     if (n_pending == kMaxPending) {  // resolve the oldest now
                         if (resolve_tile(a, pending[0], warp, lane, pending_old[0]))
-                            reduce_tile<NS, NT>(a, pending[0], warp, lane, ok);
+                            reduce_any<NS, NT, DIAG>(a, pending[0], warp, lane, ok);
                         for (int i = 1; i < kMaxPending; ++i) {
                             pending[i - 1] = pending[i];
                             pending_old[i - 1] = pending_old[i];
@@ -898,7 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
     }
     for (int i = 0; i < n_pending; ++i)
         if (resolve_tile(a, pending[i], warp, lane, pending_old[i]))
-            reduce_tile<NS, NT>(a, pending[i], warp, lane, ok);
+            reduce_any<NS, NT, DIAG>(a, pending[i], warp, lane, ok);
 }
 
 int device_sm_count() {
@@ -979,6 +1062,7 @@ cudaError_t launch_stream_gemv(int streams, const void* x, int M, int K, const v
     a.cnt_off = p.cnt_off;
     a.misc_off = p.misc_off;
     a.s_max = p.s_max;
+    a.part_stride = p.part_stride;
     a.scale_a = scale_a;
     a.scale_b = scale_b;
     a.act = act;
