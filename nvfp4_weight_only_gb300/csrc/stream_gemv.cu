@@ -49,6 +49,12 @@ constexpr int kSmemMax = 227 * 1024;
 constexpr int kXBudget = 96 * 1024;
 constexpr int kRingBudget = 200 * 1024;
 constexpr int kMaxStages = 8;
+// Up to this many tokens the split-K partials are element-major (each output
+// element's parts contiguous, read in 16-byte vectors by the last range); above
+// it the scattered 4-byte slot stores cost more than the vector reads save, and
+// each range writes one contiguous slot instead.
+constexpr int kElemMajorMaxM = 4;
+static_assert(kElemMajorMaxM >= 2, "the diagonal layout (M <= 2) writes element-major partials");
 constexpr int kMiscBytes = 512;
 constexpr int kMiscIssuesOff = 256;  // per-stage copy counts (kMaxStages ints) in the misc area
 // Chunks (of 64 K elements) summed in plain fp32 before the sum is folded into
@@ -67,7 +73,8 @@ struct Plan {
     int grid, R;
     long long Pmax;         // steps per range (max)
     int cps, xcap, x_stride, stage_bytes, stages, s_max, slot_floats;
-    int part_stride;  // diagonal layout: parts per element, padded to 4 (0 otherwise)
+    int part_stride;  // M <= kElemMajorMaxM: element-major partials, parts per element
+                      // padded to 4 (0: range-major slots)
     int x_off, bar_off, cnt_off, misc_off;
     size_t smem;
     size_t counters_off, partials_off, total;
@@ -120,7 +127,7 @@ static Plan make_plan(int NS, int M, int N, int K, int num_sms) {
     p.counters_off = 0;
     p.partials_off = (size_t)ceil_div((long long)p.RB * kBlockTiles * 4, 256) * 256;
     p.part_stride = 0;
-    if (diag) {
+    if (M <= kElemMajorMaxM) {
         // element-major: the parts of one output element are contiguous, so the
         // last range to arrive reads them with a few 16-byte loads
         long long most = 1;
@@ -166,7 +173,7 @@ struct KArgs {
     long long L;
     int M, K, N, C, CS, RB, R, grid;
     int stages, stage_bytes, x_off, x_stride, bar_off, cnt_off, misc_off, s_max;
-    int part_stride;  // diagonal layout's element-major partials (parts per element)
+    int part_stride;  // element-major partials: parts per element, padded to 4 (0: slots)
     float scale_a, scale_b;
     int act;
     int early_weights;  // stream weights before waiting on the preceding kernel
@@ -482,7 +489,7 @@ __device__ __forceinline__ bool resolve_tile(const KArgs& a, int rb, int warp, i
 // range's slot, is published (fence, then the tile's counter), and the
 // function returns true when this range arrived last for the tile and must
 // reduce it (done after the stream, by reduce_tile).
-template <int NS, int NT, bool DIAG>
+template <int NS, int NT, bool DIAG, bool EM>
 __device__ __forceinline__ int finish_segment(const KArgs& a, float (&hi)[NS][NT][4],
                                                float (&lo)[NS][NT][4],
                                                const float (&unscale)[NT][2], int r, int q0,
@@ -521,7 +528,7 @@ __device__ __forceinline__ int finish_segment(const KArgs& a, float (&hi)[NS][NT
             }
         return -1;
     }
-    if (DIAG) {
+    if (EM) {
         // element-major: element (si, row, token) of the tile, part r - r_first
         float* base = a.partials + (size_t)(rb * kBlockTiles + warp) * (NS * kTileRows * a.M) *
                                        a.part_stride +
@@ -530,7 +537,7 @@ __device__ __forceinline__ int finish_segment(const KArgs& a, float (&hi)[NS][NT
         for (int si = 0; si < NS; ++si)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int token = e & 1;
+                const int token = DIAG ? (e & 1) : 2 * tq + (e & 1);
                 if (lane_stores && token < a.M)
                     base[(size_t)((si * kTileRows + g + 8 * (e >> 1)) * a.M + token) *
                          a.part_stride] = v[si][0][e];
@@ -605,52 +612,68 @@ __device__ __forceinline__ void reduce_tile(const KArgs& a, int rb, int warp, in
 // than chained MMAs on GB300).  With two token tiles: folded into the A
 // fragments by an exact f16 multiply, so the MMAs accumulate directly and the
 // scaling is shared by both tiles.
-// reduce_tile for the diagonal layout's element-major partials: lane e owns
-// element e (< 16*M <= 32) of each stream and reads its parts in 16-byte
-// vectors, 16 parts per batch, summing them in range order.
+// reduce_tile for the element-major partials (M <= kElemMajorMaxM): lane l owns
+// elements l, l+32, ... (< 16*M) of each stream and reads each element's parts
+// in 16-byte vectors, kPB parts per batch with every load of the batch in
+// flight together, summing them in range order.
 template <int NS>
-__device__ __forceinline__ void reduce_tile_diag(const KArgs& a, int rb, int warp, int lane,
-                                                 bool ok) {
+__device__ __forceinline__ void reduce_tile_em(const KArgs& a, int rb, int warp, int lane,
+                                               bool ok) {
+    constexpr int kIter = kTileRows * kElemMajorMaxM / 32;  // elements per lane, largest M
+    constexpr int kPB = 32 / (kIter * NS);                 // parts per batch (32 in flight)
+    static_assert(kPB % 4 == 0, "parts are read in 16-byte vectors");
     const long long p_lo = (long long)rb * a.CS;
     const int nparts = range_of(a, p_lo + a.CS - 1) - range_of(a, p_lo) + 1;
     const int n_el = kTileRows * a.M;
-    const int e = lane;
-    if (e >= n_el) return;
     const float* base = a.partials + (size_t)(rb * kBlockTiles + warp) * (NS * n_el) * a.part_stride;
-    float sum[NS];
+    float sum[kIter][NS];
 #pragma unroll
-    for (int si = 0; si < NS; ++si) sum[si] = 0.0f;
-    for (int p0 = 0; p0 < nparts; p0 += 16) {
-        float part[NS][16];
+    for (int i = 0; i < kIter; ++i)
 #pragma unroll
-        for (int si = 0; si < NS; ++si) {
-            const float4* src = reinterpret_cast<const float4*>(
-                base + (size_t)(si * n_el + e) * a.part_stride + p0);
+        for (int si = 0; si < NS; ++si) sum[i][si] = 0.0f;
+    for (int p0 = 0; p0 < nparts; p0 += kPB) {
+        float part[kIter][NS][kPB];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 v4 = p0 + 4 * q < nparts ? __ldcg(src + q)
-                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-                part[si][4 * q] = v4.x;
-                part[si][4 * q + 1] = v4.y;
-                part[si][4 * q + 2] = v4.z;
-                part[si][4 * q + 3] = v4.w;
+        for (int i = 0; i < kIter; ++i) {
+            const int e = lane + 32 * i;
+#pragma unroll
+            for (int si = 0; si < NS; ++si) {
+                const float4* src = reinterpret_cast<const float4*>(
+                    base + (size_t)(si * n_el + e) * a.part_stride + p0);
+#pragma unroll
+                for (int q = 0; q < kPB / 4; ++q) {
+                    const float4 v4 = (e < n_el && p0 + 4 * q < nparts)
+                                          ? __ldcg(src + q)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                    part[i][si][4 * q] = v4.x;
+                    part[i][si][4 * q + 1] = v4.y;
+                    part[i][si][4 * q + 2] = v4.z;
+                    part[i][si][4 * q + 3] = v4.w;
+                }
             }
         }
 #pragma unroll
-        for (int si = 0; si < NS; ++si)
+        for (int i = 0; i < kIter; ++i)
 #pragma unroll
-            for (int q = 0; q < 16; ++q)
-                if (p0 + q < nparts) sum[si] += part[si][q];
+            for (int si = 0; si < NS; ++si)
+#pragma unroll
+                for (int q = 0; q < kPB; ++q)
+                    if (p0 + q < nparts) sum[i][si] += part[i][si][q];
     }
-    const int token = e % a.M, row16 = e / a.M;
-    const int row = rb * kBlockRows + warp * kTileRows + row16;
-    if (ok && row < a.N) store_output<NS>(a, row, token, sum[0], sum[NS - 1]);
+#pragma unroll
+    for (int i = 0; i < kIter; ++i) {
+        const int e = lane + 32 * i;
+        if (e >= n_el) continue;
+        const int token = e % a.M, row16 = e / a.M;
+        const int row = rb * kBlockRows + warp * kTileRows + row16;
+        if (ok && row < a.N) store_output<NS>(a, row, token, sum[i][0], sum[i][NS - 1]);
+    }
 }
 
-template <int NS, int NT, bool DIAG>
+template <int NS, int NT, bool EM>
 __device__ __forceinline__ void reduce_any(const KArgs& a, int rb, int warp, int lane, bool ok) {
-    if constexpr (DIAG)
-        reduce_tile_diag<NS>(a, rb, warp, lane, ok);
+    if constexpr (EM)
+        reduce_tile_em<NS>(a, rb, warp, lane, ok);
     else
         reduce_tile<NS, NT>(a, rb, warp, lane, ok);
 }
@@ -806,7 +829,8 @@ __device__ __forceinline__ void issue_step(const KArgs& a, const StepCursor& cur
 
 // ONE: a single token row (M == 1), which needs only the even MMA columns.
 // DIAG: M <= 2 with the diagonal token layout (stage_x_diag).
-template <int NS, int NT, bool ONE, bool DIAG>
+// EM: element-major split-K partials (M <= kElemMajorMaxM).
+template <int NS, int NT, bool ONE, bool DIAG, bool EM>
 __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a) {
     constexpr int CPS = kUnitsPerStep / NS;  // chunks per step
 
@@ -960,12 +984,12 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
                         }
             }
             if (seg_end) {
-                const int old = finish_segment<NS, NT, DIAG>(a, hi, lo, unscale, r, q0, rb_now,
+                const int old = finish_segment<NS, NT, DIAG, EM>(a, hi, lo, unscale, r, q0, rb_now,
                                                              cb_now, warp, lane, ok);
                 if (old >= 0) {
                     if (n_pending == kMaxPending) {  // resolve the oldest now
                         if (resolve_tile(a, pending[0], warp, lane, pending_old[0]))
-                            reduce_any<NS, NT, DIAG>(a, pending[0], warp, lane, ok);
+                            reduce_any<NS, NT, EM>(a, pending[0], warp, lane, ok);
                         for (int i = 1; i < kMaxPending; ++i) {
                             pending[i - 1] = pending[i];
                             pending_old[i - 1] = pending_old[i];
@@ -981,7 +1005,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
     }
     for (int i = 0; i < n_pending; ++i)
         if (resolve_tile(a, pending[i], warp, lane, pending_old[i]))
-            reduce_any<NS, NT, DIAG>(a, pending[i], warp, lane, ok);
+            reduce_any<NS, NT, EM>(a, pending[i], warp, lane, ok);
 }
 
 int device_sm_count() {
@@ -1006,13 +1030,13 @@ size_t gemv_scratch_bytes(int streams, int M, int N, int K, int num_sms) {
     return make_plan(streams, M, N, K, num_sms).total;
 }
 
-template <int NS, int NT, bool ONE, bool DIAG>
+template <int NS, int NT, bool ONE, bool DIAG, bool EM>
 static cudaError_t launch_t(const Plan& p, const KArgs& a, cudaStream_t s) {
     static bool attr_done[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(stream_gemv_kernel<NS, NT, ONE, DIAG>,
+        cudaError_t e = cudaFuncSetAttribute(stream_gemv_kernel<NS, NT, ONE, DIAG, EM>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
@@ -1027,7 +1051,7 @@ static cudaError_t launch_t(const Plan& p, const KArgs& a, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, stream_gemv_kernel<NS, NT, ONE, DIAG>, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, stream_gemv_kernel<NS, NT, ONE, DIAG, EM>, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -1071,15 +1095,19 @@ cudaError_t launch_stream_gemv(int streams, const void* x, int M, int K, const v
     a.div_R = FastDiv::make((unsigned)p.R);
     a.div_L = FastDiv::make((unsigned)(p.L < (1LL << 32) ? p.L : 1));
     a.div_CS = FastDiv::make((unsigned)p.CS);
+    const bool em = p.part_stride != 0;
     if (streams == 1) {
-        if (M == 1) return launch_t<1, 1, true, true>(p, a, s);
-        if (M == 2) return launch_t<1, 1, false, true>(p, a, s);
-        return p.NT == 1 ? launch_t<1, 1, false, false>(p, a, s)
-                         : launch_t<1, 2, false, false>(p, a, s);
+        if (M == 1) return launch_t<1, 1, true, true, true>(p, a, s);
+        if (M == 2) return launch_t<1, 1, false, true, true>(p, a, s);
+        if (em) return launch_t<1, 1, false, false, true>(p, a, s);
+        return p.NT == 1 ? launch_t<1, 1, false, false, false>(p, a, s)
+                         : launch_t<1, 2, false, false, false>(p, a, s);
     }
-    if (M == 1) return launch_t<2, 1, true, true>(p, a, s);
-    if (M == 2) return launch_t<2, 1, false, true>(p, a, s);
-    return p.NT == 1 ? launch_t<2, 1, false, false>(p, a, s) : launch_t<2, 2, false, false>(p, a, s);
+    if (M == 1) return launch_t<2, 1, true, true, true>(p, a, s);
+    if (M == 2) return launch_t<2, 1, false, true, true>(p, a, s);
+    if (em) return launch_t<2, 1, false, false, true>(p, a, s);
+    return p.NT == 1 ? launch_t<2, 1, false, false, false>(p, a, s)
+                     : launch_t<2, 2, false, false, false>(p, a, s);
 }
 
 }  // namespace nvf
