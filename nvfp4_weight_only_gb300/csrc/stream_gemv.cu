@@ -902,9 +902,6 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
     }
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    StepCursor cur;
-    cur.init(a);
-
     float acc[NS][NT][4], hi[NS][NT][4], lo[NS][NT][4];
 #pragma unroll
     for (int si = 0; si < NS; ++si)
@@ -923,10 +920,15 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
     constexpr int kMaxPending = 4;
     int pending[kMaxPending], pending_old[kMaxPending];
     int n_pending = 0;
-    while (cur.valid(a)) {
-        // ---- a new range: stage its token rows
-        const int r = cur.r, q0 = cur.q, q1 = cur.q_end;
-        const int c_start = cur.cb * CPS;
+    constexpr int kFoldSteps = kFoldChunks / CPS;  // steps between folds
+    static_assert(kFoldSteps * CPS == kFoldChunks && (kFoldSteps & (kFoldSteps - 1)) == 0,
+                  "fold period is a power-of-two number of steps");
+    for (int r = blockIdx.x; r < a.R; r += a.grid) {
+        // ---- a new range: steps q0 .. q1-1; stage its token rows
+        const int q0 = (int)range_start(a, r), q1 = (int)range_start(a, r + 1);
+        int rb = rb_of_step(a, q0);
+        int cb = q0 - rb * a.CS;
+        const int c_start = cb * CPS;
         const int nx = (q1 - q0) * CPS < a.C ? (q1 - q0) * CPS : a.C;
         consumer_sync();  // every warp is done with the previous range's x
         if (DIAG)
@@ -939,67 +941,64 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
 #pragma unroll
             for (int e = 0; e < 2; ++e)
                 unscale[nt][e] = tok_unscale[DIAG ? e : nt * 8 + 2 * tq + e];
-        int ci = 0, folded = 0;
-        while (cur.valid(a) && cur.r == r) {
-            if (ok && !mbar_wait_bounded(full0 + 8u * st, ph, abort_flag)) {
-                ok = false;
-                *abort_flag = 1;
-                atomicOr(a.status, 1);
-            }
-            if (ok) {
-                const uint8_t* stage = smem + (size_t)st * a.stage_bytes;
-#pragma unroll
-                for (int j = 0; j < CPS; ++j) {
-                    if constexpr (DIAG)
-                        process_chunk_diag<NS, ONE>(stage, xs, j, ci + j, warp, lane, scale_sel,
-                                                    acc);
-                    else
-                        process_chunk<NS, NT, ONE>(stage, xs, a.x_stride, a.M, j, ci + j, warp,
-                                                   lane, acc);
+        int ci = 0;
+        // ---- the range's segments: the run of its steps inside one row block
+        for (int q = q0; q < q1; q += a.CS - cb, ++rb, cb = 0) {
+            const int seg_n = q1 - q < a.CS - cb ? q1 - q : a.CS - cb;
+            for (int k = 0; k < seg_n; ++k) {
+                if (ok && !mbar_wait_bounded(full0 + 8u * st, ph, abort_flag)) {
+                    ok = false;
+                    *abort_flag = 1;
+                    atomicOr(a.status, 1);
                 }
-            }
-            // Release the stage to the producer.
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8u * st);
-            if (++st == a.stages) {
-                st = 0;
-                ph ^= 1u;
-            }
-            const int rb_now = cur.rb, cb_now = cur.cb;
-            cur.advance(a);
-            ci += CPS;
-            if (ci >= a.C) ci -= a.C;
-            folded += CPS;
-            const bool seg_end = (cb_now == a.CS - 1) || (cur.r != r) || !cur.valid(a);
-            if (folded >= kFoldChunks || seg_end) {
-                folded = 0;
+                if (ok) {
+                    const uint8_t* stage = smem + (size_t)st * a.stage_bytes;
 #pragma unroll
-                for (int si = 0; si < NS; ++si)
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; e += ONE ? 2 : 1) {
-                            two_sum_acc(hi[si][nt][e], lo[si][nt][e], acc[si][nt][e]);
-                            acc[si][nt][e] = 0.0f;
-                        }
-            }
-            if (seg_end) {
-                const int old = finish_segment<NS, NT, DIAG, EM>(a, hi, lo, unscale, r, q0, rb_now,
-                                                             cb_now, warp, lane, ok);
-                if (old >= 0) {
-                    if (n_pending == kMaxPending) {  // resolve the oldest now
-                        if (resolve_tile(a, pending[0], warp, lane, pending_old[0]))
-                            reduce_any<NS, NT, EM>(a, pending[0], warp, lane, ok);
-                        for (int i = 1; i < kMaxPending; ++i) {
-                            pending[i - 1] = pending[i];
-                            pending_old[i - 1] = pending_old[i];
-                        }
-                        --n_pending;
+                    for (int j = 0; j < CPS; ++j) {
+                        if constexpr (DIAG)
+                            process_chunk_diag<NS, ONE>(stage, xs, j, ci + j, warp, lane,
+                                                        scale_sel, acc);
+                        else
+                            process_chunk<NS, NT, ONE>(stage, xs, a.x_stride, a.M, j, ci + j,
+                                                       warp, lane, acc);
                     }
-                    pending[n_pending] = rb_now;
-                    pending_old[n_pending] = old;
-                    ++n_pending;
                 }
+                // Release the stage to the producer.
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty0 + 8u * st);
+                if (++st == a.stages) {
+                    st = 0;
+                    ph ^= 1u;
+                }
+                ci += CPS;
+                if (ci >= a.C) ci -= a.C;
+                if ((k & (kFoldSteps - 1)) == kFoldSteps - 1 || k == seg_n - 1) {
+#pragma unroll
+                    for (int si = 0; si < NS; ++si)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int e = 0; e < 4; e += ONE ? 2 : 1) {
+                                two_sum_acc(hi[si][nt][e], lo[si][nt][e], acc[si][nt][e]);
+                                acc[si][nt][e] = 0.0f;
+                            }
+                }
+            }
+            const int old = finish_segment<NS, NT, DIAG, EM>(a, hi, lo, unscale, r, q0, rb,
+                                                             cb + seg_n - 1, warp, lane, ok);
+            if (old >= 0) {
+                if (n_pending == kMaxPending) {  // resolve the oldest now
+                    if (resolve_tile(a, pending[0], warp, lane, pending_old[0]))
+                        reduce_any<NS, NT, EM>(a, pending[0], warp, lane, ok);
+                    for (int i = 1; i < kMaxPending; ++i) {
+                        pending[i - 1] = pending[i];
+                        pending_old[i - 1] = pending_old[i];
+                    }
+                    --n_pending;
+                }
+                pending[n_pending] = rb;
+                pending_old[n_pending] = old;
+                ++n_pending;
             }
         }
     }
