@@ -55,8 +55,14 @@ constexpr int kMaxStages = 8;
 // each range writes one contiguous slot instead.
 constexpr int kElemMajorMaxM = 4;
 static_assert(kElemMajorMaxM >= 2, "the diagonal layout (M <= 2) writes element-major partials");
-constexpr int kMiscBytes = 512;
-constexpr int kMiscIssuesOff = 256;  // per-stage copy counts (kMaxStages ints) in the misc area
+// The misc area: token scales and amax (0..), the abort flag, the per-stage
+// copy counts (kMiscIssuesOff), then the publication area (kMiscPubOff):
+// kMaxEvents "segment stored" mbarriers (count kWarps), kMaxEvents
+// "published" mbarriers (count 1) and the returned counts, kWarps per event.
+constexpr int kMaxEvents = 8;
+constexpr int kMiscIssuesOff = 256;  // per-stage copy counts (kMaxStages ints)
+constexpr int kMiscPubOff = 512;
+constexpr int kMiscBytes = kMiscPubOff + 16 * kMaxEvents + 4 * 16 * kMaxEvents;
 // Chunks (of 64 K elements) summed in plain fp32 before the sum is folded into
 // the exact hi/lo pair.
 constexpr int kFoldChunks = 8;
@@ -468,6 +474,22 @@ __device__ __forceinline__ int publish_tile(const KArgs& a, int rb, int warp, in
     return old;  // lane 0 only; consumed later by resolve_tile
 }
 
+// The counter's old value for a pending publication `p` of this warp (lane 0):
+// p >= 0 is the value itself; p <= -2 is publisher event -2 - p, whose value is
+// read once the publisher has marked the event done.  Returns -1 (and flags
+// the call) if that wait is abandoned.
+__device__ __forceinline__ int pending_old_value(const KArgs& a, int p, int warp,
+                                                 uint32_t pub_done0, const int* pub_old,
+                                                 const volatile int* abort_flag) {
+    if (p >= 0) return p;
+    const int e = -2 - p;
+    if (!mbar_wait_bounded(pub_done0 + 8u * e, 0, abort_flag)) {
+        atomicOr(a.status, 1);
+        return -1;
+    }
+    return pub_old[e * kWarps + warp];
+}
+
 // Whether the publication that returned `old` (lane 0) was the last of the
 // ranges covering rb; the last one resets the counter for the next call.
 __device__ __forceinline__ bool resolve_tile(const KArgs& a, int rb, int warp, int lane, int old) {
@@ -475,7 +497,7 @@ __device__ __forceinline__ bool resolve_tile(const KArgs& a, int rb, int warp, i
     if (lane == 0) {
         const long long p_lo = (long long)rb * a.CS;
         const int nparts = range_of(a, p_lo + a.CS - 1) - range_of(a, p_lo) + 1;
-        last = (old == nparts - 1) ? 1 : 0;
+        last = (old >= 0 && old == nparts - 1) ? 1 : 0;
         if (last) a.counters[rb * kBlockTiles + warp] = 0;  // ready for the next call
     }
     last = __shfl_sync(0xffffffffu, last, 0);
@@ -485,15 +507,18 @@ __device__ __forceinline__ bool resolve_tile(const KArgs& a, int rb, int warp, i
 
 // End of the segment of row block rb (last step cb_last) that range r covers,
 // for this warp's tile; no CTA-wide synchronisation.  A segment spanning the
-// whole K range is stored at once.  Otherwise the fp32 partial goes to the
-// range's slot, is published (fence, then the tile's counter), and the
-// function returns true when this range arrived last for the tile and must
-// reduce it (done after the stream, by reduce_tile).
+// whole K range is stored at once (returns -1).  Otherwise the fp32 partial
+// goes to the range's slot and is counted in on the tile's counter: for the
+// CTA's first kMaxEvents such segments (event evt) by the publisher warp,
+// asynchronously (returns -2 - evt), later ones by this warp (returns the
+// counter's old value, lane 0).  Whether this range arrived last, and so must
+// reduce the tile, is resolved after the stream (resolve_pending).
 template <int NS, int NT, bool DIAG, bool EM>
 __device__ __forceinline__ int finish_segment(const KArgs& a, float (&hi)[NS][NT][4],
                                                float (&lo)[NS][NT][4],
                                                const float (&unscale)[NT][2], int r, int q0,
-                                               int rb, int cb_last, int warp, int lane, bool ok) {
+                                               int rb, int cb_last, int warp, int lane, bool ok,
+                                               int evt, uint32_t seg_done0) {
     const int g = lane >> 2, tq = lane & 3;
     const int seg_lo = q0 > rb * a.CS ? q0 : rb * a.CS;
     const bool full_cover = (seg_lo == rb * a.CS) && (cb_last == a.CS - 1);
@@ -556,6 +581,13 @@ __device__ __forceinline__ int finish_segment(const KArgs& a, float (&hi)[NS][NT
                 }
     }
     __syncwarp();
+    if (evt < kMaxEvents) {
+        // the publisher warp counts the tile in once every warp has stored;
+        // this warp streams on (the arrive releases the lanes' slot stores to
+        // the CTA, and the publisher's GPU-scope release carries them on)
+        if (lane == 0) mbar_arrive(seg_done0 + 8u * evt);
+        return -2 - evt;
+    }
     return publish_tile(a, rb, warp, lane);
 }
 
@@ -843,6 +875,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
     unsigned* amax_u = reinterpret_cast<unsigned*>(tok_unscale + 16);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(amax_u + 16);
     int* issues = reinterpret_cast<int*>(smem + a.misc_off + kMiscIssuesOff);  // copies per stage
+    const uint32_t seg_done0 = smem_addr(smem + a.misc_off + kMiscPubOff);  // per event
+    const uint32_t pub_done0 = seg_done0 + 8u * kMaxEvents;
+    int* pub_old = reinterpret_cast<int*>(smem + a.misc_off + kMiscPubOff + 16 * kMaxEvents);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tq = lane & 3;
@@ -854,6 +889,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
             mbar_init(full0 + 8u * s, 1);
             mbar_init(empty0 + 8u * s, kWarps);
             issues[s] = 0;
+        }
+        for (int e = 0; e < kMaxEvents; ++e) {
+            mbar_init(seg_done0 + 8u * e, kWarps);
+            mbar_init(pub_done0 + 8u * e, 1);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -897,6 +936,33 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
             for (int s = 0; s < a.stages; ++s)
                 if (issues[s] > 0)
                     mbar_wait_bounded(full0 + 8u * s, (uint32_t)((issues[s] - 1) & 1), &zero);
+        } else if (warp == kWarps + 1) {
+            // ---- publisher: counts the consumer warps' partial tiles in on the
+            // split-K counters, so that the GPU-scope release of the slot
+            // stores (which waits for them to reach L2) holds up this warp and
+            // not the stream.  The segments are enumerated as the consumers
+            // walk them; lane t < kWarps handles tile t.
+            int e = 0;
+            for (int r = blockIdx.x; r < a.R && e < kMaxEvents; r += a.grid) {
+                const int q0 = (int)range_start(a, r), q1 = (int)range_start(a, r + 1);
+                int rb = rb_of_step(a, q0);
+                int cb = q0 - rb * a.CS;
+                for (int q = q0; q < q1 && e < kMaxEvents; q += a.CS - cb, ++rb, cb = 0) {
+                    const int seg_n = q1 - q < a.CS - cb ? q1 - q : a.CS - cb;
+                    if (cb == 0 && seg_n == a.CS) continue;  // whole row block: stored directly
+                    if (!mbar_wait_bounded(seg_done0 + 8u * e, 0, abort_flag)) {
+                        *abort_flag = 1;
+                        atomicOr(a.status, 1);
+                        return;
+                    }
+                    if (lane < kWarps)
+                        pub_old[e * kWarps + lane] =
+                            atom_add_acq_rel_gpu(a.counters + rb * kBlockTiles + lane, 1);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(pub_done0 + 8u * e);
+                    ++e;
+                }
+            }
         }
         return;
     }
@@ -920,6 +986,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
     constexpr int kMaxPending = 4;
     int pending[kMaxPending], pending_old[kMaxPending];
     int n_pending = 0;
+    int evt = 0;  // partial segments so far (publisher events)
     constexpr int kFoldSteps = kFoldChunks / CPS;  // steps between folds
     static_assert(kFoldSteps * CPS == kFoldChunks && (kFoldSteps & (kFoldSteps - 1)) == 0,
                   "fold period is a power-of-two number of steps");
@@ -985,10 +1052,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
                 }
             }
             const int old = finish_segment<NS, NT, DIAG, EM>(a, hi, lo, unscale, r, q0, rb,
-                                                             cb + seg_n - 1, warp, lane, ok);
-            if (old >= 0) {
+                                                             cb + seg_n - 1, warp, lane, ok, evt,
+                                                             seg_done0);
+            if (old != -1) {
+                ++evt;
                 if (n_pending == kMaxPending) {  // resolve the oldest now
-                    if (resolve_tile(a, pending[0], warp, lane, pending_old[0]))
+                    const int o = pending_old_value(a, pending_old[0], warp, pub_done0, pub_old,
+                                                    abort_flag);
+                    if (resolve_tile(a, pending[0], warp, lane, o))
                         reduce_any<NS, NT, EM>(a, pending[0], warp, lane, ok);
                     for (int i = 1; i < kMaxPending; ++i) {
                         pending[i - 1] = pending[i];
@@ -1002,9 +1073,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
             }
         }
     }
-    for (int i = 0; i < n_pending; ++i)
-        if (resolve_tile(a, pending[i], warp, lane, pending_old[i]))
+    for (int i = 0; i < n_pending; ++i) {
+        const int o = pending_old_value(a, pending_old[i], warp, pub_done0, pub_old, abort_flag);
+        if (resolve_tile(a, pending[i], warp, lane, o))
             reduce_any<NS, NT, EM>(a, pending[i], warp, lane, ok);
+    }
 }
 
 int device_sm_count() {
