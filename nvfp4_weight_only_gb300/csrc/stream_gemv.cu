@@ -49,11 +49,11 @@ constexpr int kSmemMax = 227 * 1024;
 constexpr int kXBudget = 96 * 1024;
 constexpr int kRingBudget = 200 * 1024;
 constexpr int kMaxStages = 8;
-// Up to this many tokens the split-K partials are element-major (each output
-// element's parts contiguous, read in 16-byte vectors by the last range); above
-// it the scattered 4-byte slot stores cost more than the vector reads save, and
-// each range writes one contiguous slot instead.
-constexpr int kElemMajorMaxM = 4;
+// Up to this many tokens (one MMA token group) the split-K partials are
+// element-major: each output element's parts are contiguous, and the last
+// range reads them in 16-byte vectors.  With two token groups (M > 8) each
+// range writes one contiguous slot instead.
+constexpr int kElemMajorMaxM = 8;
 static_assert(kElemMajorMaxM >= 2, "the diagonal layout (M <= 2) writes element-major partials");
 // The misc area: token scales and amax (0..), the abort flag, the per-stage
 // copy counts (kMiscIssuesOff), then the publication area (kMiscPubOff):
@@ -243,7 +243,10 @@ struct StepCursor {
 // fp32, act(g) = g to fp32 precision while the exact act(g) is slightly
 // smaller in magnitude; g*u is then exact in fp32, and an exact bf16 tie of
 // it must round toward zero, as the exact product (strictly inside) does.
-__device__ __forceinline__ __nv_bfloat16 gated_product(int act, float g, float u) {
+// Not inlined: the last range's epilogue runs it for several elements per lane
+// right after the stream, and one shared copy of its code costs one round of
+// instruction fetch misses instead of one per unrolled element.
+__device__ __noinline__ __nv_bfloat16 gated_product(int act, float g, float u) {
     const float y = (act == 0) ? g : 1.5957691216057308f * (g + 0.044715f * g * g * g);
     if (y < 0.0f) {
         const float e = expf(y);
@@ -644,14 +647,14 @@ __device__ __forceinline__ void reduce_tile(const KArgs& a, int rb, int warp, in
 // than chained MMAs on GB300).  With two token tiles: folded into the A
 // fragments by an exact f16 multiply, so the MMAs accumulate directly and the
 // scaling is shared by both tiles.
-// reduce_tile for the element-major partials (M <= kElemMajorMaxM): lane l owns
-// elements l, l+32, ... (< 16*M) of each stream and reads each element's parts
-// in 16-byte vectors, kPB parts per batch with every load of the batch in
-// flight together, summing them in range order.
-template <int NS>
+// reduce_tile for the element-major partials (M <= MAXM): lane l owns elements
+// l, l+32, ... (< 16*M) of each stream and reads each element's parts in
+// 16-byte vectors, kPB parts per batch with every load of the batch in flight
+// together, summing them in range order.
+template <int NS, int MAXM>
 __device__ __forceinline__ void reduce_tile_em(const KArgs& a, int rb, int warp, int lane,
                                                bool ok) {
-    constexpr int kIter = kTileRows * kElemMajorMaxM / 32;  // elements per lane, largest M
+    constexpr int kIter = (kTileRows * MAXM + 31) / 32;  // elements per lane at the largest M
     constexpr int kPB = 32 / (kIter * NS);                 // parts per batch (32 in flight)
     static_assert(kPB % 4 == 0, "parts are read in 16-byte vectors");
     const long long p_lo = (long long)rb * a.CS;
@@ -702,10 +705,10 @@ __device__ __forceinline__ void reduce_tile_em(const KArgs& a, int rb, int warp,
     }
 }
 
-template <int NS, int NT, bool EM>
+template <int NS, int NT, bool DIAG, bool EM>
 __device__ __forceinline__ void reduce_any(const KArgs& a, int rb, int warp, int lane, bool ok) {
     if constexpr (EM)
-        reduce_tile_em<NS>(a, rb, warp, lane, ok);
+        reduce_tile_em<NS, DIAG ? 2 : kElemMajorMaxM>(a, rb, warp, lane, ok);
     else
         reduce_tile<NS, NT>(a, rb, warp, lane, ok);
 }
@@ -1060,7 +1063,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
                     const int o = pending_old_value(a, pending_old[0], warp, pub_done0, pub_old,
                                                     abort_flag);
                     if (resolve_tile(a, pending[0], warp, lane, o))
-                        reduce_any<NS, NT, EM>(a, pending[0], warp, lane, ok);
+                        reduce_any<NS, NT, DIAG, EM>(a, pending[0], warp, lane, ok);
                     for (int i = 1; i < kMaxPending; ++i) {
                         pending[i - 1] = pending[i];
                         pending_old[i - 1] = pending_old[i];
@@ -1076,7 +1079,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
     for (int i = 0; i < n_pending; ++i) {
         const int o = pending_old_value(a, pending_old[i], warp, pub_done0, pub_old, abort_flag);
         if (resolve_tile(a, pending[i], warp, lane, o))
-            reduce_any<NS, NT, EM>(a, pending[i], warp, lane, ok);
+            reduce_any<NS, NT, DIAG, EM>(a, pending[i], warp, lane, ok);
     }
 }
 
