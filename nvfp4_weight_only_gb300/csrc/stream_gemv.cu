@@ -285,31 +285,46 @@ __device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float b) {
 // Barrier over the consumer warps only (the producer warp never joins).
 __device__ __forceinline__ void consumer_sync() { named_barrier_sync(1, kConsumerThreads); }
 
-// Per token m (threads 0..15): the exponent e_m with amax_m * 2^e_m in
-// [2^14, 2^15), kept biased in amax_u[m] for the conversion pass, and the
-// unscale factor 2^-e_m for the fp32 results.
-__device__ __forceinline__ void token_scales(unsigned* amax_u, float* tok_unscale) {
-    const int tid = threadIdx.x;
-    if (tid < 16) {
-        const float am = __uint_as_float(amax_u[tid]);
-        int e = 0;
-        if (am > 0.0f) {
-            int ex;
-            frexpf(am, &ex);  // am < 2^ex, so am * 2^(15-ex) lies in [2^14, 2^15)
-            e = 15 - ex;
-            e = e < -100 ? -100 : (e > 100 ? 100 : e);
-        }
-        amax_u[tid] = (unsigned)(e + 128);  // reuse: biased exponent for the second pass
-        tok_unscale[tid] = __int_as_float((127 - e) << 23);
+// The exponent e of a token with absolute maximum amax (bit pattern): amax *
+// 2^e lies in [2^14, 2^15), clamped to +-100; 0 for an all-zero token.
+__device__ __forceinline__ int token_exponent(unsigned amax_bits) {
+    const float am = __uint_as_float(amax_bits);
+    int e = 0;
+    if (am > 0.0f) {
+        int ex;
+        frexpf(am, &ex);  // am < 2^ex, so am * 2^(15-ex) lies in [2^14, 2^15)
+        e = 15 - ex;
+        e = e < -100 ? -100 : (e > 100 ? 100 : e);
     }
+    return e;
 }
 
-// bf16 pair -> f16 pair scaled by 2^(biased - 128) (exact for the range kept).
-__device__ __forceinline__ uint32_t scale_pair_to_f16(uint32_t pr, unsigned biased) {
-    const float sc = __int_as_float(((int)biased - 128 + 127) << 23);
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+// bf16 pair -> f16 pair scaled by sc = 2^e (exact for the range kept).
+__device__ __forceinline__ uint32_t scale_pair_to_f16(uint32_t pr, float sc) {
     const __half2 hv = __floats2half2_rn(__uint_as_float(pr << 16) * sc,
                                          __uint_as_float(pr & 0xFFFF0000u) * sc);
     return *reinterpret_cast<const uint32_t*>(&hv);
+}
+
+__device__ __forceinline__ void track_amax(float& mx, const uint4& v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        mx = fmaxf(mx, fabsf(__uint_as_float(w[i] << 16)));
+        mx = fmaxf(mx, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+    }
+}
+
+// The 16-byte group q (8 k values) of token m's rows for chunks c_start ...
+// (mod C), or zeros past K.
+__device__ __forceinline__ uint4 load_x_group(const KArgs& a, int m, int c_start, int q) {
+    int c = c_start + (q >> 3);
+    if (c >= a.C) c -= a.C;
+    const int k0 = c * kChunkK + (q & 7) * 8;
+    if (k0 >= a.K) return make_uint4(0u, 0u, 0u, 0u);
+    return __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)m * a.K + k0));
 }
 
 // Stage the token rows for chunks c_start .. c_start+nx-1 (mod C) into shared
@@ -317,15 +332,17 @@ __device__ __forceinline__ uint32_t scale_pair_to_f16(uint32_t pr, unsigned bias
 // m and chunk ci, 128 bytes at m*x_stride + ci*128, where lane quarter t owns
 // 32 bytes = the k pairs (16j+2t, +1) and (16j+2t+8, +9) of blocks j = 0..3.
 // One coalesced global pass (16-byte loads) scatters the bf16 values into
-// place and tracks each token's amax; a second, shared-memory-only pass scales
-// token m by 2^e_m (amax * 2^e_m in [2^14, 2^15)) and rounds to f16, which is
-// exact for every bf16 value within 2^-24 of the row's amax.
+// place and tracks each token's amax; after one barrier a shared-memory-only
+// pass scales token m by 2^e_m (amax * 2^e_m in [2^14, 2^15)) and rounds to
+// f16, which is exact for every bf16 value within 2^-24 of the row's amax.
+// (The scattered 4-byte stores conflict on banks; issued before the barrier
+// they hide behind the other warps' loads, and the conversion pass is
+// conflict-free 16-byte accesses.)  amax_u[0..15] is zero on entry and left
+// zero.
 template <int NT>
 __device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float* tok_unscale,
                         unsigned* amax_u) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid < 16) amax_u[tid] = 0u;
-    consumer_sync();
     // Warps are dealt to tokens, wpt per token, so that every index below is
     // a shift or an add and a token's amax is one warp reduction.
     const int wpt = kWarps / a.M;
@@ -334,7 +351,6 @@ __device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float*
     const int stride = wpt * 32;
     float mx_local = 0.0f;
     if (m < a.M) {
-        const __nv_bfloat16* xrow = a.x + (size_t)m * a.K;
         uint8_t* row = xs + m * a.x_stride;
         // A lane's groups go in rounds of kLoads: all loads of a round are in
         // flight together before any value is used.
@@ -344,28 +360,18 @@ __device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float*
 #pragma unroll
             for (int u = 0; u < kLoads; ++u) {
                 const int q = base + u * stride;
-                v[u] = make_uint4(0u, 0u, 0u, 0u);
-                if (q < per_token) {
-                    int c = c_start + (q >> 3);
-                    if (c >= a.C) c -= a.C;
-                    const int k0 = c * kChunkK + (q & 7) * 8;
-                    if (k0 < a.K) v[u] = __ldg(reinterpret_cast<const uint4*>(xrow + k0));
-                }
+                v[u] = q < per_token ? load_x_group(a, m, c_start, q) : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
             for (int u = 0; u < kLoads; ++u) {
                 const int q = base + u * stride;
                 if (q >= per_token) break;
-                const int ci = q >> 3, grp = q & 7;  // grp: k0 = 8*grp within the chunk
-                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    mx_local = fmaxf(mx_local, fabsf(__uint_as_float(w[i] << 16)));
-                    mx_local = fmaxf(mx_local, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
-                }
+                track_amax(mx_local, v[u]);
                 // pair i (k = k0 + 2i, +1) belongs to lane quarter t = i, block
                 // j = grp/2, half = grp&1 (b0 for k%16 < 8, b1 otherwise)
+                const int ci = q >> 3, grp = q & 7;
                 uint8_t* dst = row + ci * 128 + (grp >> 1) * 8 + (grp & 1) * 4;
+                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) *reinterpret_cast<uint32_t*>(dst + i * 32) = w[i];
             }
@@ -375,21 +381,21 @@ __device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float*
     const unsigned wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(mx_local));
     if (lane == 0 && m < a.M && wmax != 0u) atomicMax(&amax_u[m], wmax);
     consumer_sync();
-    token_scales(amax_u, tok_unscale);
-    consumer_sync();
+    if (tid < 16) tok_unscale[tid] = pow2f(-token_exponent(amax_u[tid]));
     if (m < a.M) {  // exact power-of-two f16 conversion, 16 bytes per lane
         uint4* row = reinterpret_cast<uint4*>(xs + m * a.x_stride);
-        const unsigned biased = amax_u[m];
-        for (int i = wi * 32 + lane; i < nx * 8; i += stride) {
+        const float sc = pow2f(token_exponent(amax_u[m]));
+        for (int i = wi * 32 + lane; i < per_token; i += stride) {
             uint4 w = row[i];
-            w.x = scale_pair_to_f16(w.x, biased);
-            w.y = scale_pair_to_f16(w.y, biased);
-            w.z = scale_pair_to_f16(w.z, biased);
-            w.w = scale_pair_to_f16(w.w, biased);
+            w.x = scale_pair_to_f16(w.x, sc);
+            w.y = scale_pair_to_f16(w.y, sc);
+            w.z = scale_pair_to_f16(w.z, sc);
+            w.w = scale_pair_to_f16(w.w, sc);
             row[i] = w;
         }
     }
     consumer_sync();
+    if (tid < 16) amax_u[tid] = 0u;  // for the next range (after its opening barrier)
 }
 
 // Token rows for one or two tokens ("diagonal" B operand).  The 8 columns of
@@ -400,57 +406,56 @@ __device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float*
 // 1024 bytes at ci*1024 hold, for lane L = 4g + t, the B registers of the four
 // MMAs: bytes h*512 + 16L + 4r (h = j/2, r = 2(j%2) + b) are the pair
 // (x[m][16j + 2t + 8b], +1) when g = 2j + m with m < M, and zero otherwise.
-// Same two passes as stage_x (coalesced load + scatter + amax, then an exact
-// power-of-two f16 conversion), after a zero fill of the chunks.
+// As stage_x: the loads are issued first, the area is zero-filled while they
+// are in flight, and after the amax barrier each lane converts its groups and
+// writes their words over the zeros.
 __device__ void stage_x_diag(const KArgs& a, uint8_t* xs, int c_start, int nx, float* tok_unscale,
                              unsigned* amax_u) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid < 16) amax_u[tid] = 0u;
-    for (int i = tid; i < nx * 64; i += kConsumerThreads)
-        reinterpret_cast<uint4*>(xs)[i] = make_uint4(0u, 0u, 0u, 0u);
-    consumer_sync();
     const int wpt = kWarps / a.M;  // warps per token (M <= 2)
     const int m = warp / wpt, wi = warp - m * wpt;
     const int per_token = nx * 8;  // 16-byte groups of 8 k per token
     const int stride = wpt * 32;
+    const int q0 = wi * 32 + lane;
+    constexpr int kLoads = 2;  // 64 chunks of 8 groups over 256 lanes (M = 2)
+    const bool in_regs = per_token <= kLoads * stride;
     float mx_local = 0.0f;
-    for (int q = wi * 32 + lane; q < per_token; q += stride) {
-        const int ci = q >> 3, grp = q & 7;  // k0 = 8*grp within the chunk
-        int c = c_start + ci;
-        if (c >= a.C) c -= a.C;
-        const int k0 = c * kChunkK + grp * 8;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (k0 < a.K) v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)m * a.K + k0));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint4 v[kLoads];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            mx_local = fmaxf(mx_local, fabsf(__uint_as_float(w[i] << 16)));
-            mx_local = fmaxf(mx_local, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
-        }
-        // pair i (k = 8*grp + 2i): block j = grp/2, half b = grp&1, quarter t = i
-        const int j = grp >> 1, b = grp & 1;
-        uint8_t* dst = xs + ci * 1024 + (j >> 1) * 512 + (4 * (2 * j + m)) * 16 + 4 * (2 * (j & 1) + b);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) *reinterpret_cast<uint32_t*>(dst + 16 * i) = w[i];
+    for (int u = 0; u < kLoads; ++u) {
+        const int q = q0 + u * stride;
+        v[u] = q < per_token ? load_x_group(a, m, c_start, q) : make_uint4(0u, 0u, 0u, 0u);
     }
+    for (int i = tid; i < nx * 64; i += kConsumerThreads)  // overlaps the loads
+        reinterpret_cast<uint4*>(xs)[i] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) track_amax(mx_local, v[u]);
+    for (int q = q0 + kLoads * stride; q < per_token; q += stride)  // beyond the registers
+        track_amax(mx_local, load_x_group(a, m, c_start, q));
     const unsigned wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(mx_local));
     if (lane == 0 && wmax != 0u) atomicMax(&amax_u[m], wmax);
-    consumer_sync();
-    token_scales(amax_u, tok_unscale);
-    consumer_sync();
-    // convert the token's non-zero words: per chunk, block j and quarter t, the
-    // two words (b = 0, 1) at lane 4(2j + m) + t
-    const unsigned biased = amax_u[m];
-    for (int it = wi * 32 + lane; it < nx * 16; it += stride) {
-        const int ci = it >> 4, j = (it >> 2) & 3, t = it & 3;
-        uint2* p = reinterpret_cast<uint2*>(xs + ci * 1024 + (j >> 1) * 512 +
-                                            (4 * (2 * j + m) + t) * 16 + 8 * (j & 1));
-        uint2 w = *p;
-        w.x = scale_pair_to_f16(w.x, biased);
-        w.y = scale_pair_to_f16(w.y, biased);
-        *p = w;
+    consumer_sync();  // amax complete; zero fill ordered before the data words
+    if (tid < 16) tok_unscale[tid] = pow2f(-token_exponent(amax_u[tid]));
+    const float sc = pow2f(token_exponent(amax_u[m]));
+    for (int base = q0; base < per_token; base += kLoads * stride) {
+#pragma unroll
+        for (int u = 0; u < kLoads; ++u) {
+            const int q = base + u * stride;
+            if (q >= per_token) break;
+            const uint4 w4 = in_regs ? v[u] : load_x_group(a, m, c_start, q);
+            const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+            // pair i (k = 8*grp + 2i): block j = grp/2, half b = grp&1, quarter t = i
+            const int ci = q >> 3, grp = q & 7;
+            const int j = grp >> 1, b = grp & 1;
+            uint8_t* dst =
+                xs + ci * 1024 + (j >> 1) * 512 + (4 * (2 * j + m)) * 16 + 4 * (2 * (j & 1) + b);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<uint32_t*>(dst + 16 * i) = scale_pair_to_f16(w[i], sc);
+        }
     }
     consumer_sync();
+    if (tid < 16) amax_u[tid] = 0u;  // for the next range (after its opening barrier)
 }
 
 // Split-K bookkeeping of one warp's tile.  Slot (range r, segment index) holds,
@@ -897,6 +902,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
             mbar_init(seg_done0 + 8u * e, kWarps);
             mbar_init(pub_done0 + 8u * e, 1);
         }
+        for (int t = 0; t < 16; ++t) amax_u[t] = 0u;  // staging's token maxima
         *abort_flag = 0;
         fence_mbar_init();
     }
