@@ -738,13 +738,13 @@ __device__ __forceinline__ void process_chunk(const uint8_t* stage, const uint8_
     uint32_t b[NT][8];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        const int token = nt * 8 + g;  // B column (token row of x) this lane supplies
-        uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
-        if (token < M) {
-            const uint8_t* px = xs + token * x_stride + cj * 128 + tq * 32;
-            v0 = *reinterpret_cast<const uint4*>(px);
-            v1 = *reinterpret_cast<const uint4*>(px + 16);
-        }
+        // B column (token row of x) this lane supplies.  Columns past the last
+        // token repeat its row: their sums land in output columns that are
+        // never stored, and every load stays inside the staged rows.
+        const int token = min(nt * 8 + g, M - 1);
+        const uint8_t* px = xs + token * x_stride + cj * 128 + tq * 32;
+        const uint4 v0 = *reinterpret_cast<const uint4*>(px);
+        const uint4 v1 = *reinterpret_cast<const uint4*>(px + 16);
         b[nt][0] = v0.x;
         b[nt][1] = v0.y;
         b[nt][2] = v0.z;
