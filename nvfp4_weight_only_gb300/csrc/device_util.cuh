@@ -141,6 +141,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
     return r;
 }
 
+// The same for the high two bytes of v (bytes 2, 3).
+__device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t v) {
+    uint32_t r;
+    asm("{\n .reg .b16 lo, h;\n mov.b32 {lo, h}, %1;\n cvt.rn.f16x2.e4m3x2 %0, h;\n}"
+        : "=r"(r)
+        : "r"(v));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
     uint32_t r;
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));

@@ -766,8 +766,8 @@ __device__ __forceinline__ void process_chunk(const uint8_t* stage, const uint8_
             uint32_t a0, a1, a2, a3;
             e2m1x8_to_f16x2x4(cws[jb], a0, a1, a2, a3);
             const uint32_t sword = jb < 2 ? sw.x : sw.y;
-            const uint32_t sp = (jb & 1) ? (sword >> 16) : sword;
-            const uint32_t s2 = e4m3x2_to_f16x2(sp);  // (row g, row g+8) scales
+            const uint32_t s2 = (jb & 1) ? e4m3x2_hi_to_f16x2(sword)
+                                         : e4m3x2_to_f16x2(sword);  // (row g, row g+8) scales
             if (kScaleInA<NT>()) {
                 // (s_g, s_g) and (s_g8, s_g8) as f16x2; an E4M3 value times an
                 // E2M1 value is exact in f16 (at most 6 significant bits,
