@@ -199,6 +199,27 @@ def test_gemv_largest_sweep_shape_sampled_rows(dev):
     assert_close(y[:, torch.from_numpy(rows).to(dev)], ref, "gemv 65536x21504 sampled rows")
 
 
+def test_gemv_many_ranges_per_cta_sampled_rows(dev):
+    """N=65536, K=10240, M=16: with two token groups the staged token rows
+    limit a range to 11 steps, so each CTA walks about seven ranges and up to
+    nine partial segments.  Some CTAs therefore pass the publisher warp's
+    eight events and count the rest in-warp, and resolve pending tiles early.
+    The oracle quantises the whole weight; 640 rows are checked against its
+    GEMV of just those rows."""
+    N, K, M = 65536, 10240, 16
+    w = synth.weights_f32(N, K, seed=78)
+    rc, rs, rs2 = oracle.quantize(w.numpy())
+    del w
+    p = ffi.nvfp4_repack(torch.from_numpy(rc).to(dev), torch.from_numpy(rs).to(dev), N, K)
+    x = synth.activations_bf16(M, K, seed=6, outlier_frac=0.01)
+    y = ffi.nvfp4_gemv(x.to(dev), p, float(rs2), N)
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([np.arange(64), np.arange(N - 64, N),
+                                     rng.choice(N, 512, replace=False)]))
+    ref = oracle.gemv(synth.bf16_bits(x), rc[rows], rs[rows], rs2, len(rows))
+    assert_close(y[:, torch.from_numpy(rows).to(dev)], ref, "gemv 65536x10240 M=16 sampled rows")
+
+
 # ------------------------------------------------------------------ FFN
 
 def build_ffn(dev, H, I, layer=0):
