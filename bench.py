@@ -11,7 +11,11 @@ L2, so every step streams weights from HBM.
 
 Prints ONE JSON line (rank 0).  `value` is the effective HBM bandwidth of the
 whole job: algorithmic bytes (3*H*I*0.5625 weight bytes + 2*M*H*2 activation
-bytes per layer) / device time, summed over ranks.
+bytes per layer) / device time, summed over ranks.  On one GPU the line also
+carries `sweep`: the same metric for M = 1..16 on the headline layer (with the
+gate/up and down kernels timed on their own), the 1%-outlier batch-M variants
+with SiLU and GeLU, the speculative-verify and large dense layers, and points of
+the standalone GEMV sweep (`--no-sweep` skips it).
 """
 import argparse
 import hashlib
@@ -168,6 +172,61 @@ def dist_setup():
 
 # ---------------------------------------------------------------------- our arm
 
+def build_layers(ffi, synth, H, I, L, dev, seed_offset=0):
+    """Quantise + repack L distinct FFN layers on the device (load time, untimed)."""
+    import torch
+
+    layers = []
+    for li in range(L):
+        q = []
+        for proj, (n, k) in ((synth.GATE, (I, H)), (synth.UP, (I, H)), (synth.DOWN, (H, I))):
+            w = synth.weights_f32(n, k, seed=synth.layer_seed(li, proj) + seed_offset, device=dev)
+            q.append(ffi.nvfp4_quantize(w))
+            del w
+        gu = ffi.nvfp4_repack_gate_up(q[0][0], q[0][1], q[1][0], q[1][1], I, H)
+        dn = ffi.nvfp4_repack(q[2][0], q[2][1], H, I)
+        layers.append((gu, q[0][2], q[1][2], dn, q[2][2]))
+        del q
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return layers
+
+
+class GraphTimer:
+    """Captures a callable into a CUDA graph on one stream and times replays
+    with CUDA events recorded on that stream."""
+
+    def __init__(self, stream):
+        self.stream = stream
+
+    def capture(self, fn):
+        import torch
+
+        with torch.cuda.stream(self.stream):
+            fn()  # first launch sets kernel attributes outside capture
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                fn()
+        torch.cuda.synchronize()
+        return g
+
+    def time(self, graph, reps, warmup=0):
+        import torch
+
+        with torch.cuda.stream(self.stream):
+            for _ in range(warmup):
+                graph.replay()
+            ev0 = torch.cuda.Event(enable_timing=True)
+            ev1 = torch.cuda.Event(enable_timing=True)
+            ev0.record(self.stream)
+            for _ in range(reps):
+                graph.replay()
+            ev1.record(self.stream)
+        ev1.synchronize()
+        return ev0.elapsed_time(ev1) / 1e3
+
+
 def run_ours(args, wl):
     import torch
     import torch.distributed as dist
@@ -184,19 +243,7 @@ def run_ours(args, wl):
     act = wl["act"] if args.act is None else args.act
 
     # ---- load time: quantise + repack every layer on the device (untimed)
-    layers = []
-    for li in range(L):
-        q = []
-        for proj, (n, k) in ((synth.GATE, (I, H)), (synth.UP, (I, H)), (synth.DOWN, (H, I))):
-            w = synth.weights_f32(n, k, seed=synth.layer_seed(li, proj) + 7919 * rank, device=dev)
-            q.append(ffi.nvfp4_quantize(w))
-            del w
-        gu = ffi.nvfp4_repack_gate_up(q[0][0], q[0][1], q[1][0], q[1][1], I, H)
-        dn = ffi.nvfp4_repack(q[2][0], q[2][1], H, I)
-        layers.append((gu, q[0][2], q[1][2], dn, q[2][2]))
-        del q
-    torch.cuda.synchronize()
-    torch.cuda.empty_cache()
+    layers = build_layers(ffi, synth, H, I, L, dev, seed_offset=7919 * rank)
     x = synth.activations_bf16(M, H, seed=0, outlier_frac=wl["outliers"], device=dev)
     out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
     ws = ffi.workspace(ffi.ffn_swiglu_nvfp4_workspace_bytes(M, H, I), dev)
@@ -217,27 +264,9 @@ def run_ours(args, wl):
             ffi.nvfp4_gemv(h, dn, d2, H, ws=ws_dn, out=out)
 
     stream = torch.cuda.Stream(device=dev)
-    graphs = {}
-    with torch.cuda.stream(stream):
-        for name, fn in (("step", step), ("dual", dual_only), ("down", down_only)):
-            fn()  # first launch sets kernel attributes outside capture
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                fn()
-            graphs[name] = g
-    torch.cuda.synchronize()
-
-    def timed(graph, reps):
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for _ in range(reps):
-                graph.replay()
-            ev1.record(stream)
-        ev1.synchronize()
-        return ev0.elapsed_time(ev1) / 1e3
+    timer = GraphTimer(stream)
+    graphs = {name: timer.capture(fn)
+              for name, fn in (("step", step), ("dual", dual_only), ("down", down_only))}
 
     # ---- warm-up, then the timed region (barrier + sync on both sides)
     for _ in range(args.warmup):
@@ -254,21 +283,17 @@ def run_ours(args, wl):
         dist.barrier()
     torch.cuda.synchronize()
     w0 = time.time()
-    t_step = timed(graphs["step"], args.steps)
+    t_step = timer.time(graphs["step"], args.steps)
     torch.cuda.synchronize()
     sampler.mark(w0, time.time())
     if world > 1:
         dist.barrier()
     # per-kernel averages (same process, same stream, CUDA events)
     kreps = max(3, min(args.steps, 200))
-    for _ in range(2):
-        graphs["dual"].replay()
     w0 = time.time()
-    t_dual = timed(graphs["dual"], kreps) / (kreps * L)
-    t_down = timed(graphs["down"], kreps) / (kreps * L)
+    t_dual = timer.time(graphs["dual"], kreps, warmup=2) / (kreps * L)
+    t_down = timer.time(graphs["down"], kreps, warmup=2) / (kreps * L)
     sampler.mark(w0, time.time())
-    time.sleep(0.15)
-    clocks = sampler.stop()
 
     # ---- end to end through the public API with host buffers
     x_host = x.cpu().pin_memory()
@@ -292,23 +317,15 @@ def run_ours(args, wl):
     t_e2e_eager = ev0.elapsed_time(ev1) / 1e3 / e2e_steps
 
     # The same step as a serving loop would run it: the pinned-host copy of x,
-    # the 48 public-API calls and the read-back of out, captured once into a
-    # CUDA graph and replayed (the calls only enqueue work on the stream).
-    with torch.cuda.stream(stream):
-        g_e2e = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_e2e, stream=stream):
-            x.copy_(x_host, non_blocking=True)
-            step()
-            out_host.copy_(out, non_blocking=True)
-        for _ in range(2):
-            g_e2e.replay()
-        stream.synchronize()
-        ev0.record(stream)
-        for _ in range(e2e_steps):
-            g_e2e.replay()
-        ev1.record(stream)
-        ev1.synchronize()
-    t_e2e = ev0.elapsed_time(ev1) / 1e3 / e2e_steps
+    # the per-layer public-API calls and the read-back of out, captured once
+    # into a CUDA graph and replayed (the calls only enqueue work on the stream).
+    def e2e_step():
+        x.copy_(x_host, non_blocking=True)
+        step()
+        out_host.copy_(out, non_blocking=True)
+
+    g_e2e = timer.capture(e2e_step)
+    t_e2e = timer.time(g_e2e, e2e_steps, warmup=2) / e2e_steps
     status = ffi.nvfp4_workspace_status(ws)
     if status != 0:
         raise RuntimeError(f"device status word reports {status} (bounded wait abandoned)")
@@ -326,6 +343,15 @@ def run_ours(args, wl):
         if (tr.get("source_hash") == kernel_source_hash() and tr.get("H") == H
                 and tr.get("I") == I and tr.get("M") == M):
             traffic = tr.get("bytes_per_launch")
+
+    # ---- the metric's whole M range and the other configured shapes (one GPU)
+    sweep, sweep_launches = None, 0
+    if world == 1 and not args.no_sweep:
+        sweep, sweep_launches = run_sweep(args, ffi, synth, dev, timer, sampler, layers, H, I,
+                                          peak)
+    time.sleep(0.15)
+    clocks = sampler.stop()
+
     line = None
     if rank == 0:
         line = {
@@ -362,9 +388,132 @@ def run_ours(args, wl):
             "gpu_launches": 2 * L * args.steps,
             "clocks": clocks,
         }
+        if sweep is not None:
+            line["sweep"] = sweep
+            line["sweep_gpu_launches"] = sweep_launches
     if world > 1:
         dist.barrier()
     return line
+
+
+def _layer_entry(t_layer, H, I, M, peak):
+    gbs = layer_bytes(H, I, M) / t_layer / 1e9
+    return {"us_per_layer": round(t_layer * 1e6, 3), "gbs": round(gbs, 1),
+            "frac": round(gbs / peak, 4)}
+
+
+def run_sweep(args, ffi, synth, dev, timer, sampler, layers, H, I, peak):
+    """M = 1..16 on the headline layer (with per-kernel times), the batch-M
+    outlier variants (SiLU and GeLU), the speculative-verify layer, the large
+    dense layer and points of the standalone GEMV sweep.  Every entry is a CUDA
+    graph of all its distinct layers (or weight copies), larger than L2,
+    replayed `--sweep-reps` times after warm-up and timed with CUDA events."""
+    import torch
+
+    reps = args.sweep_reps
+    launches = 0
+    res = {"reps": reps, "note": "µs per layer, effective GB/s and fraction of the measured "
+                                 "HBM copy peak; per-kernel figures for the headline layer"}
+
+    def ffn_case(lyrs, H, I, M, act, outliers, kernels=False):
+        nonlocal launches
+        x = synth.activations_bf16(M, H, seed=M, outlier_frac=outliers, device=dev)
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        ws = ffi.workspace(ffi.ffn_swiglu_nvfp4_workspace_bytes(M, H, I), dev)
+
+        def fn():
+            for (gu, g2, u2, dn, d2) in lyrs:
+                ffi.ffn_swiglu_nvfp4(x, gu, g2, u2, dn, d2, I, act, ws=ws, out=out)
+
+        g = timer.capture(fn)
+        w0 = time.time()
+        t = timer.time(g, reps, warmup=3) / (reps * len(lyrs))
+        launches += 2 * len(lyrs) * reps
+        entry = _layer_entry(t, H, I, M, peak)
+        if kernels:
+            h = torch.empty((M, I), dtype=torch.bfloat16, device=dev)
+            ws_gu = ffi.workspace(ffi.ffn_gate_up_nvfp4_workspace_bytes(M, H, I), dev)
+            ws_dn = ffi.workspace(ffi.nvfp4_gemv_workspace_bytes(M, H, I), dev)
+
+            def dual():
+                for (gu, g2, u2, dn, d2) in lyrs:
+                    ffi.ffn_gate_up_nvfp4(x, gu, g2, u2, I, act, ws=ws_gu, h=h)
+
+            def down():
+                for (gu, g2, u2, dn, d2) in lyrs:
+                    ffi.nvfp4_gemv(h, dn, d2, H, ws=ws_dn, out=out)
+
+            for name, f, nbytes in (("dual", dual, dual_kernel_bytes(H, I, M)),
+                                    ("down", down, down_kernel_bytes(H, I, M))):
+                gk = timer.capture(f)
+                tk = timer.time(gk, reps, warmup=3) / (reps * len(lyrs))
+                launches += len(lyrs) * reps
+                entry[name] = {"us_per_launch": round(tk * 1e6, 3),
+                               "frac": round(nbytes / tk / 1e9 / peak, 4)}
+                del gk
+            if ffi.nvfp4_workspace_status(ws_gu) != 0 or ffi.nvfp4_workspace_status(ws_dn) != 0:
+                raise RuntimeError("device status word reports a bounded wait abandoned")
+        sampler.mark(w0, time.time())
+        if ffi.nvfp4_workspace_status(ws) != 0:
+            raise RuntimeError("device status word reports a bounded wait abandoned")
+        del g
+        return entry
+
+    head = {}
+    for M in range(1, 17):
+        head[f"M{M}"] = ffn_case(layers, H, I, M, 0, 0.0, kernels=True)
+    res[f"ffn_{H}x{I}_silu"] = head
+    bm = {}
+    for M in (4, 8, 16):
+        for act, name in ((0, "silu"), (1, "gelu_tanh")):
+            bm[f"M{M}_{name}"] = ffn_case(layers, H, I, M, act, 0.01)
+    res[f"ffn_{H}x{I}_outliers_1pct"] = bm
+    torch.cuda.empty_cache()
+
+    for key, Hs, Is, Ls, Ms in (("spec_verify", 4096, 12288, 32, (2, 3)),
+                                ("large", 5376, 21504, 62, (1, 2, 4, 8, 12, 16))):
+        lyrs = build_layers(ffi, synth, Hs, Is, Ls, dev)
+        res[f"{key}_{Hs}x{Is}"] = {f"M{M}": ffn_case(lyrs, Hs, Is, M, 0, 0.0) for M in Ms}
+        del lyrs
+        torch.cuda.empty_cache()
+
+    # standalone nvfp4_gemv: enough identical weight copies (distinct addresses)
+    # to exceed 2 GB, so every launch streams from HBM
+    gem = {}
+    for (N, K) in ((4096, 4096), (17408, 5120), (5120, 17408), (65536, 4096), (4096, 21504),
+                   (65536, 21504)):
+        w = synth.weights_f32(N, K, seed=N + K, device=dev)
+        c, s, s2 = ffi.nvfp4_quantize(w)
+        del w
+        p = ffi.nvfp4_repack(c, s, N, K)
+        del c, s
+        nbytes = N * K * 0.5625
+        copies = int(min(256, max(3, -(-2.2e9 // nbytes))))
+        ps = [p] + [p.clone() for _ in range(copies - 1)]
+        for M in (1, 4, 8, 16):
+            x = synth.activations_bf16(M, K, seed=M, device=dev)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ws = ffi.workspace(ffi.nvfp4_gemv_workspace_bytes(M, N, K), dev)
+
+            def fn():
+                for pc in ps:
+                    ffi.nvfp4_gemv(x, pc, s2, N, ws=ws, out=y)
+
+            g = timer.capture(fn)
+            w0 = time.time()
+            t = timer.time(g, reps, warmup=3) / (reps * copies)
+            sampler.mark(w0, time.time())
+            launches += copies * reps
+            gbs = (nbytes + M * K * 2 + M * N * 2) / t / 1e9
+            gem[f"N{N}_K{K}_M{M}"] = {"us_per_launch": round(t * 1e6, 3), "gbs": round(gbs, 1),
+                                      "frac": round(gbs / peak, 4), "copies": copies}
+            if ffi.nvfp4_workspace_status(ws) != 0:
+                raise RuntimeError("device status word reports a bounded wait abandoned")
+            del g
+        del ps, p
+        torch.cuda.empty_cache()
+    res["gemv"] = gem
+    return res, launches
 
 
 def cpu_baseline(wl, M, budget_s=10.0):
@@ -438,6 +587,9 @@ def main():
     ap.add_argument("--layers", type=int, default=None,
                     help="distinct layers (fewer only for small profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the M=1..16 / other-shape sweep (one GPU only)")
+    ap.add_argument("--sweep-reps", type=int, default=10)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
