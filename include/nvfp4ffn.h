@@ -130,9 +130,12 @@ nvfp4_status nvfp4_unpack(const void* packed, int N, int K, uint8_t* codes,
 
 /*
  * Workspace bytes for nvfp4_gemv on the current device (cross-CTA partial
- * sums and their counters).  The workspace must be zero-filled once after it
- * is allocated (cudaMemset or nvfp4_workspace_init); every successful call
- * leaves it ready for the next one.
+ * sums and their counters); 0 for invalid sizes or N > 524288.
+ * Workspace contract (all GEMV/FFN calls): zero-fill the workspace once after
+ * it is allocated (cudaMemset or nvfp4_workspace_init).  Every call that
+ * completes normally leaves it ready for the next one, whatever the next
+ * call's entry point and shape, provided the workspace is large enough for
+ * that call.  Calls sharing one workspace must be ordered (one stream).
  */
 size_t nvfp4_gemv_workspace_bytes(int M, int N, int K);
 
@@ -152,9 +155,13 @@ nvfp4_status nvfp4_gemv(const void* x, int M, int K, const void* packed_w, float
 /* ------------------------------------------------------------------ FFN */
 
 /* Workspace bytes for ffn_swiglu_nvfp4 on the current device: the bf16
- * activation h [M, I] plus the partial sums of both kernels.  Zero-fill once
- * after allocation, as for nvfp4_gemv. */
+ * activation h [M, I] plus the partial sums of both kernels (0 for invalid
+ * sizes or I + H above about 524288).  Contract as for nvfp4_gemv. */
 size_t ffn_swiglu_nvfp4_workspace_bytes(int M, int H, int I);
+
+/* Byte offset inside an ffn_swiglu_nvfp4 workspace of the bf16 activation
+ * h [M, I] (row-major) that the call leaves there (an inspection aid). */
+size_t ffn_swiglu_nvfp4_hidden_offset(void);
 
 /*
  * The decode FFN (DenseFfnLayer::forward and forward_km on the dense-FFN
@@ -200,17 +207,36 @@ nvfp4_status ffn_gate_up_nvfp4(const void* x, int M, int H, int I, const void* g
  *   that loads the library until the process exits.  Shapes whose
  *   ffn_swiglu_nvfp4_workspace_bytes exceeds 24 MiB are rejected with
  *   NVFP4_ERR_WORKSPACE (M = 16 at H = 5376, I = 21504 needs about 21 MiB).
- *   The first call on each device resolves the array's device address
- *   (cudaGetSymbolAddress); make that first call before any stream capture.
- *   Each call zero-fills the part of the array it uses on `stream` and then
- *   runs the two FFN kernels there; it allocates nothing.  Every call shares
- *   the one array, so calls that overlap on the GPU (different streams without
- *   ordering between them) race and corrupt each other's results.
+ *   Every argument is checked before anything is touched: a rejected call
+ *   changes nothing on the device.
+ *   The first call on each device (with that device current) resolves the
+ *   array's device address (cudaGetSymbolAddress) and zero-fills the array on
+ *   `stream`, synchronising it; make that first call before any stream
+ *   capture.  Later calls only enqueue the two FFN kernels on `stream`: like
+ *   ffn_swiglu_nvfp4's workspace, the array is left ready for the next call by
+ *   every call that completes normally.  The call allocates nothing.
+ *   Every call shares the one array, so calls that overlap on the GPU
+ *   (different streams without ordering between them) race and corrupt each
+ *   other's results.
+ *   A call whose kernel abandoned a bounded wait is reported only by
+ *   nvfp4_noalloc_status, which also repairs the array; until it is called,
+ *   later calls may return wrong results.
  */
 nvfp4_status ffn_swiglu_nvfp4_noalloc(const void* x, int M, int H, int I,
                                       const void* gate_up_packed, float gate_scale2,
                                       float up_scale2, const void* down_packed, float down_scale2,
                                       nvfp4_act act, void* out, cudaStream_t stream);
+
+/*
+ * Status of ffn_swiglu_nvfp4_noalloc calls on the current device, the
+ * counterpart of nvfp4_workspace_status for the library's fixed array (no
+ * counterpart on the pages).  Synchronises `stream`, reads and clears the
+ * array's status word: NVFP4_OK, or NVFP4_ERR_TIMEOUT when a kernel abandoned
+ * a bounded wait since the last check, in which case the whole array is
+ * zero-filled again (on `stream`, synchronised) so the next call starts clean.
+ * Performs the first-call set-up if no call has yet run on this device.
+ */
+nvfp4_status nvfp4_noalloc_status(cudaStream_t stream);
 
 /* ------------------------------------------------------------------ utilities */
 
@@ -220,7 +246,9 @@ nvfp4_status nvfp4_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream
 /*
  * Synchronises `stream`, then reads and clears the device status word at the
  * start of a GEMV/FFN workspace: NVFP4_OK, or NVFP4_ERR_TIMEOUT when a kernel
- * abandoned a bounded wait since the last check.
+ * abandoned a bounded wait since the last check.  A kernel that gave up may
+ * leave the workspace's split-K counters off zero: after NVFP4_ERR_TIMEOUT,
+ * zero-fill the workspace again (nvfp4_workspace_init) before reusing it.
  */
 nvfp4_status nvfp4_workspace_status(void* ws, cudaStream_t stream);
 

@@ -28,7 +28,8 @@ def _nvcc():
 
 def _deps():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(ROOT, "include", "nvfp4ffn.h"))
+    inc = os.path.join(ROOT, "include")
+    files += [os.path.join(inc, f) for f in os.listdir(inc)]
     files.append(os.path.abspath(__file__))
     return max(os.path.getmtime(f) for f in files)
 

@@ -7,6 +7,7 @@
 #include "internal.h"
 #include "layout.h"
 #include "nvfp4ffn.h"
+#include "nvfp4ffn_testing.h"
 
 namespace {
 
@@ -30,23 +31,51 @@ nvfp4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : N
 
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
-// FFN workspace: [status][h (M x I bf16)][dual-kernel scratch][down-kernel scratch]
+// GEMV workspace: [status][counter region][partials].  0 if N has more row
+// blocks than the counter region holds.
+size_t gemv_ws_bytes(int streams, int M, int N, int K, int sms) {
+    if (nvf::gemv_counter_bytes(N) > nvf::kCounterRegionBytes) return 0;
+    return nvf::kDataOffset + round256(nvf::gemv_partial_bytes(streams, M, N, K, sms));
+}
+
+// FFN workspace: [status][counter region: dual's counters, then down's]
+// [h (M x I bf16)][dual-kernel partials][down-kernel partials]
 struct FfnLayout {
-    size_t h_off, dual_off, dual_bytes, down_off, down_bytes, total;
+    size_t down_cnt_off, h_off, dual_off, dual_bytes, down_off, down_bytes, total;
+    bool fits;  // both kernels' counters fit the counter region
 };
 
 FfnLayout ffn_layout(int M, int H, int I, int sms) {
     FfnLayout l;
-    l.h_off = nvf::kStatusBytes;
+    l.down_cnt_off = nvf::gemv_counter_bytes(I);
+    l.fits = l.down_cnt_off + nvf::gemv_counter_bytes(H) <= nvf::kCounterRegionBytes;
+    l.h_off = nvf::kDataOffset;
     l.dual_off = l.h_off + round256((size_t)M * I * 2);
-    l.dual_bytes = round256(nvf::gemv_scratch_bytes(2, M, I, H, sms));
+    l.dual_bytes = round256(nvf::gemv_partial_bytes(2, M, I, H, sms));
     l.down_off = l.dual_off + l.dual_bytes;
-    l.down_bytes = round256(nvf::gemv_scratch_bytes(1, M, H, I, sms));
+    l.down_bytes = round256(nvf::gemv_partial_bytes(1, M, H, I, sms));
     l.total = l.down_off + l.down_bytes;
     return l;
 }
 
 }  // namespace
+
+namespace nvf {
+
+int validate_ffn_args(const void* x, int M, int H, int I, const void* gate_up_packed,
+                      const void* down_packed, int act, const void* out) {
+    if (!x || !gate_up_packed || !down_packed || !out) return NVFP4_ERR_NULL;
+    if (M < 1 || M > 16) return NVFP4_ERR_RANGE;
+    if (act != NVFP4_ACT_SILU && act != NVFP4_ACT_GELU_TANH) return NVFP4_ERR_RANGE;
+    if (H < 16 || I < 16 || H % 16 != 0 || I % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(gate_up_packed) || !aligned16(down_packed) ||
+        !aligned16(out))
+        return NVFP4_ERR_ALIGN;
+    if (overlap(x, (size_t)M * H * 2, out, (size_t)M * H * 2)) return NVFP4_ERR_ALIAS;
+    return NVFP4_OK;
+}
+
+}  // namespace nvf
 
 extern "C" {
 
@@ -119,7 +148,7 @@ nvfp4_status nvfp4_unpack(const void* packed, int N, int K, uint8_t* codes, uint
 
 size_t nvfp4_gemv_workspace_bytes(int M, int N, int K) {
     if (M < 1 || M > 16 || N < 1 || K < 16) return 0;
-    return nvf::kStatusBytes + round256(nvf::gemv_scratch_bytes(1, M, N, K, sms_for_sizing()));
+    return gemv_ws_bytes(1, M, N, K, sms_for_sizing());
 }
 
 nvfp4_status nvfp4_gemv(const void* x, int M, int K, const void* packed_w, float scale2, int N,
@@ -132,50 +161,54 @@ nvfp4_status nvfp4_gemv(const void* x, int M, int K, const void* packed_w, float
     if (overlap(x, (size_t)M * K * 2, y, (size_t)M * N * 2)) return NVFP4_ERR_ALIAS;
     const int sms = nvf::device_sm_count();
     if (sms <= 0) return NVFP4_ERR_CUDA;
-    const size_t need = nvf::kStatusBytes + round256(nvf::gemv_scratch_bytes(1, M, N, K, sms));
+    const size_t need = gemv_ws_bytes(1, M, N, K, sms);
+    if (need == 0) return NVFP4_ERR_SHAPE;
     if (ws_bytes < need) return NVFP4_ERR_WORKSPACE;
     char* w = reinterpret_cast<char*>(ws);
-    return cuda_status(nvf::launch_stream_gemv(1, x, M, K, packed_w, N, scale2, scale2, 0, y,
-                                               reinterpret_cast<int*>(w), w + nvf::kStatusBytes,
-                                               need - nvf::kStatusBytes, sms, true, stream));
+    return cuda_status(nvf::launch_stream_gemv(
+        1, x, M, K, packed_w, N, scale2, scale2, 0, y, reinterpret_cast<int*>(w),
+        reinterpret_cast<int*>(w + nvf::kStatusBytes), w + nvf::kDataOffset,
+        need - nvf::kDataOffset, sms, true, stream));
 }
 
 size_t ffn_swiglu_nvfp4_workspace_bytes(int M, int H, int I) {
     if (M < 1 || M > 16 || H < 16 || I < 16) return 0;
-    return ffn_layout(M, H, I, sms_for_sizing()).total;
+    const FfnLayout l = ffn_layout(M, H, I, sms_for_sizing());
+    return l.fits ? l.total : 0;
 }
+
+size_t ffn_swiglu_nvfp4_hidden_offset(void) { return nvf::kDataOffset; }
 
 nvfp4_status ffn_swiglu_nvfp4(const void* x, int M, int H, int I, const void* gate_up_packed,
                               float gate_scale2, float up_scale2, const void* down_packed,
                               float down_scale2, nvfp4_act act, void* out, void* ws,
                               size_t ws_bytes, cudaStream_t stream) {
-    if (!x || !gate_up_packed || !down_packed || !out || !ws) return NVFP4_ERR_NULL;
-    if (M < 1 || M > 16) return NVFP4_ERR_RANGE;
-    if (act != NVFP4_ACT_SILU && act != NVFP4_ACT_GELU_TANH) return NVFP4_ERR_RANGE;
-    if (H < 16 || I < 16 || H % 16 != 0 || I % 16 != 0) return NVFP4_ERR_SHAPE;
-    if (!aligned16(x) || !aligned16(gate_up_packed) || !aligned16(down_packed) ||
-        !aligned16(out) || !aligned16(ws))
-        return NVFP4_ERR_ALIGN;
-    if (overlap(x, (size_t)M * H * 2, out, (size_t)M * H * 2)) return NVFP4_ERR_ALIAS;
+    if (!ws) return NVFP4_ERR_NULL;
+    const int v = nvf::validate_ffn_args(x, M, H, I, gate_up_packed, down_packed, (int)act, out);
+    if (v != NVFP4_OK) return (nvfp4_status)v;
+    if (!aligned16(ws)) return NVFP4_ERR_ALIGN;
     const int sms = nvf::device_sm_count();
     if (sms <= 0) return NVFP4_ERR_CUDA;
     const FfnLayout l = ffn_layout(M, H, I, sms);
+    if (!l.fits) return NVFP4_ERR_SHAPE;
     if (ws_bytes < l.total) return NVFP4_ERR_WORKSPACE;
     char* w = reinterpret_cast<char*>(ws);
     int* status = reinterpret_cast<int*>(w);
+    int* counters = reinterpret_cast<int*>(w + nvf::kStatusBytes);
     void* h = w + l.h_off;
     cudaError_t e = nvf::launch_stream_gemv(2, x, M, H, gate_up_packed, I, gate_scale2, up_scale2,
-                                            (int)act, h, status, w + l.dual_off, l.dual_bytes, sms,
-                                            true, stream);
+                                            (int)act, h, status, counters, w + l.dual_off,
+                                            l.dual_bytes, sms, true, stream);
     if (e != cudaSuccess) return NVFP4_ERR_CUDA;
     e = nvf::launch_stream_gemv(1, h, M, I, down_packed, H, down_scale2, down_scale2, 0, out,
-                                status, w + l.down_off, l.down_bytes, sms, true, stream);
+                                status, counters + l.down_cnt_off / sizeof(int), w + l.down_off,
+                                l.down_bytes, sms, true, stream);
     return cuda_status(e);
 }
 
 size_t ffn_gate_up_nvfp4_workspace_bytes(int M, int H, int I) {
     if (M < 1 || M > 16 || H < 16 || I < 16) return 0;
-    return nvf::kStatusBytes + round256(nvf::gemv_scratch_bytes(2, M, I, H, sms_for_sizing()));
+    return gemv_ws_bytes(2, M, I, H, sms_for_sizing());
 }
 
 nvfp4_status ffn_gate_up_nvfp4(const void* x, int M, int H, int I, const void* gate_up_packed,
@@ -190,13 +223,14 @@ nvfp4_status ffn_gate_up_nvfp4(const void* x, int M, int H, int I, const void* g
     if (overlap(x, (size_t)M * H * 2, h, (size_t)M * I * 2)) return NVFP4_ERR_ALIAS;
     const int sms = nvf::device_sm_count();
     if (sms <= 0) return NVFP4_ERR_CUDA;
-    const size_t need = nvf::kStatusBytes + round256(nvf::gemv_scratch_bytes(2, M, I, H, sms));
+    const size_t need = gemv_ws_bytes(2, M, I, H, sms);
+    if (need == 0) return NVFP4_ERR_SHAPE;
     if (ws_bytes < need) return NVFP4_ERR_WORKSPACE;
     char* w = reinterpret_cast<char*>(ws);
-    return cuda_status(nvf::launch_stream_gemv(2, x, M, H, gate_up_packed, I, gate_scale2,
-                                               up_scale2, (int)act, h, reinterpret_cast<int*>(w),
-                                               w + nvf::kStatusBytes, need - nvf::kStatusBytes,
-                                               sms, true, stream));
+    return cuda_status(nvf::launch_stream_gemv(
+        2, x, M, H, gate_up_packed, I, gate_scale2, up_scale2, (int)act, h,
+        reinterpret_cast<int*>(w), reinterpret_cast<int*>(w + nvf::kStatusBytes),
+        w + nvf::kDataOffset, need - nvf::kDataOffset, sms, true, stream));
 }
 
 nvfp4_status nvfp4_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
@@ -213,6 +247,22 @@ nvfp4_status nvfp4_workspace_status(void* ws, cudaStream_t stream) {
     if (st == 0) return NVFP4_OK;
     if (cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return NVFP4_ERR_CUDA;
     return NVFP4_ERR_TIMEOUT;
+}
+
+nvfp4_status nvfp4_testing_inject_stall(int enable, unsigned long long wait_limit_ns) {
+    if (!enable) {
+        nvf::set_test_stall(0, 1000000000ull);
+        return NVFP4_OK;
+    }
+    if (wait_limit_ns < 1000ull || wait_limit_ns > 1000000000ull) return NVFP4_ERR_RANGE;
+    nvf::set_test_stall(1, wait_limit_ns);
+    return NVFP4_OK;
+}
+
+int nvfp4_testing_plan_aligned(int streams, int M, int N, int K, int num_sms) {
+    if ((streams != 1 && streams != 2) || M < 1 || M > 16 || N < 1 || K < 16 || num_sms < 1)
+        return -1;
+    return nvf::gemv_plan_aligned(streams, M, N, K, num_sms) ? 1 : 0;
 }
 
 const char* nvfp4_status_string(nvfp4_status status) {

@@ -67,17 +67,18 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t par
 constexpr uint32_t kSuspendHintNs = 20000;
 
 // Waits for the phase with the given parity to complete.  Gives up (returns
-// false) after kWaitLimitNs, or when *abort is set by another warp (noticed
+// false) after limit_ns, or when *abort is set by another warp (noticed
 // within one suspension).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  const volatile int* abort) {
+                                                  const volatile int* abort,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
     const unsigned long long t0 = global_timer_ns();
     for (;;) {
         if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
         if (*abort) return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
 }
 

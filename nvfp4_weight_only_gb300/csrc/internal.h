@@ -17,15 +17,38 @@ cudaError_t launch_unpack(const uint8_t* packed, int N, int K, uint8_t* codes, u
                           cudaStream_t s);
 
 // stream_gemv.cu
-// Byte layout of a GEMV/FFN workspace: [status word area][...].
+// Every GEMV/FFN workspace starts with a status word area, then one fixed
+// region that holds nothing but split-K counters (one int per (row block,
+// tile) of each kernel).  Successful calls leave every counter at zero, and no
+// call writes anything else there, so a workspace zero-filled once serves any
+// sequence of shapes.  Partial sums (and the FFN's h) follow the region.
 constexpr size_t kStatusBytes = 256;
+constexpr size_t kCounterRegionBytes = 128u << 10;
+constexpr size_t kDataOffset = kStatusBytes + kCounterRegionBytes;
 
-size_t gemv_scratch_bytes(int streams, int M, int N, int K, int num_sms);
+// fp32 partial-sum bytes of one launch, and the counter bytes for N rows.
+size_t gemv_partial_bytes(int streams, int M, int N, int K, int num_sms);
+size_t gemv_counter_bytes(int N);
 cudaError_t launch_stream_gemv(int streams, const void* x, int M, int K, const void* packed, int N,
                                float scale_a, float scale_b, int act, void* out, int* status,
-                               void* scratch, size_t scratch_bytes, int num_sms, bool early_weights,
-                               cudaStream_t s);
+                               int* counters, void* partials, size_t partial_bytes, int num_sms,
+                               bool early_weights, cudaStream_t s);
 
 int device_sm_count();
+
+// Whether the kernel's shared-memory plan for this problem has the alignment
+// its accesses assume (the launcher refuses plans that do not).
+bool gemv_plan_aligned(int streams, int M, int N, int K, int num_sms);
+
+// Testing only: with stall != 0 every later GEMV/FFN launch runs with a
+// producer that issues no copies and bounded waits of wait_ns, so each
+// launch abandons its first wait and reports NVFP4_ERR_TIMEOUT.
+void set_test_stall(int stall, unsigned long long wait_ns);
+
+// Host-side argument checks of ffn_swiglu_nvfp4 that do not involve the
+// workspace (shared by the fixed-workspace entry point); 0 = OK, else an
+// nvfp4_status value.
+int validate_ffn_args(const void* x, int M, int H, int I, const void* gate_up_packed,
+                      const void* down_packed, int act, const void* out);
 
 }  // namespace nvf

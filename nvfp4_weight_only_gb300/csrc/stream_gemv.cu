@@ -12,9 +12,10 @@
 //   * persistent grid, one CTA of 16 warps per SM; warp w owns the 16-row
 //     tile w of every 256-row block of the repacked weight (layout.h);
 //   * weights stream through a ring of shared-memory stages filled by the
-//     bulk-copy (TMA) engine, completion tracked by one mbarrier per stage;
-//     the last warp to finish with a stage refills it with the step that lies
-//     a full ring ahead, so no warp ever blocks to produce;
+//     bulk-copy (TMA) engine: one lane of a producer warpgroup issues every
+//     copy, a "full" mbarrier per stage completes on the copy's bytes and an
+//     "empty" mbarrier on the 16 consumer warps' release, so the consumers
+//     never issue copies and never wait for one another;
 //   * per k16 block a warp turns its 4 code bytes into exact f16 A fragments
 //     (one cvt per E2M1 pair), runs mma.sync m16n8k16 against the token rows
 //     (B operand, staged once per range in shared memory as f16 after an exact
@@ -28,6 +29,8 @@
 // Every mbarrier wait is bounded (device status word + abort flag), and a CTA
 // that gave up waits (bounded) for its own bulk copies before it exits.
 #include <cuda_bf16.h>
+
+#include <atomic>
 
 #include "device_util.cuh"
 #include "internal.h"
@@ -83,7 +86,8 @@ struct Plan {
                       // padded to 4 (0: range-major slots)
     int x_off, bar_off, cnt_off, misc_off;
     size_t smem;
-    size_t counters_off, partials_off, total;
+    size_t counter_bytes;  // split-K counters: one int per (row block, tile)
+    size_t total;          // fp32 partial sums
 };
 
 static Plan make_plan(int NS, int M, int N, int K, int num_sms) {
@@ -124,14 +128,13 @@ static Plan make_plan(int NS, int M, int N, int K, int num_sms) {
     p.x_off = (int)(ceil_div((long long)p.stages * p.stage_bytes, 128) * 128);
     p.bar_off = (int)(ceil_div((long long)p.x_off + x_bytes, 16) * 16);
     p.cnt_off = p.bar_off + 8 * p.stages;
-    p.misc_off = p.cnt_off + (int)(ceil_div(8LL * p.stages, 16) * 16);
+    p.misc_off = (int)(ceil_div((long long)p.cnt_off + 8LL * p.stages, 128) * 128);
     p.smem = (size_t)p.misc_off + kMiscBytes;
     long long smax = ceil_div(p.Pmax, p.CS) + 1;
     if (smax > p.RB) smax = p.RB;
     p.s_max = (int)smax;
     p.slot_floats = kBlockTiles * NS * kTileRows * M;
-    p.counters_off = 0;
-    p.partials_off = (size_t)ceil_div((long long)p.RB * kBlockTiles * 4, 256) * 256;
+    p.counter_bytes = (size_t)ceil_div((long long)p.RB * kBlockTiles * 4, 256) * 256;
     p.part_stride = 0;
     if (M <= kElemMajorMaxM) {
         // element-major: the parts of one output element are contiguous, so the
@@ -143,12 +146,23 @@ static Plan make_plan(int NS, int M, int N, int K, int num_sms) {
             if (parts > most) most = parts;
         }
         p.part_stride = (int)ceil_div(most, 4) * 4;
-        p.total = p.partials_off +
-                  (size_t)p.RB * p.slot_floats * (size_t)p.part_stride * sizeof(float);
+        p.total = (size_t)p.RB * p.slot_floats * (size_t)p.part_stride * sizeof(float);
     } else {
-        p.total = p.partials_off + (size_t)p.R * p.s_max * p.slot_floats * sizeof(float);
+        p.total = (size_t)p.R * p.s_max * p.slot_floats * sizeof(float);
     }
     return p;
+}
+
+// Whether the shared-memory carve-up has the alignment every access assumes:
+// bulk-copy destinations (ring stages) and 16-byte vector loads (token rows,
+// x_stride) on 16 bytes, mbarriers on 8, the misc area (float, int and
+// mbarrier words, read as vectors nowhere today) on 128, and the whole inside
+// the per-CTA limit.  The launcher refuses a plan that fails it.
+static bool plan_aligned(const Plan& p) {
+    return p.stage_bytes % 128 == 0 && p.x_off % 128 == 0 && p.x_stride % 16 == 0 &&
+           p.bar_off % 16 == 0 && p.cnt_off % 8 == 0 && p.misc_off % 128 == 0 &&
+           kMiscIssuesOff % 16 == 0 && kMiscPubOff % 16 == 0 && p.smem <= (size_t)kSmemMax &&
+           p.stages >= 2 && p.stages <= kMaxStages;
 }
 
 // Division by a fixed divisor d >= 1 of numerators below 2^32, by a multiply:
@@ -183,6 +197,10 @@ struct KArgs {
     float scale_a, scale_b;
     int act;
     int early_weights;  // stream weights before waiting on the preceding kernel
+    // Longest bounded wait (ns).  `stall` (testing only) makes the producer
+    // issue no copies, so the consumers' first wait runs out after wait_ns.
+    unsigned long long wait_ns;
+    int stall;
     // L * R < 2^32: the range arithmetic below runs on FastDiv multiplies
     int fast;
     FastDiv div_R, div_L, div_CS;
@@ -491,7 +509,7 @@ __device__ __forceinline__ int pending_old_value(const KArgs& a, int p, int warp
                                                  const volatile int* abort_flag) {
     if (p >= 0) return p;
     const int e = -2 - p;
-    if (!mbar_wait_bounded(pub_done0 + 8u * e, 0, abort_flag)) {
+    if (!mbar_wait_bounded(pub_done0 + 8u * e, 0, abort_flag, a.wait_ns)) {
         atomicOr(a.status, 1);
         return -1;
     }
@@ -922,10 +940,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
             StepCursor ahead;
             ahead.init(a);
             int pst = 0, round = 0;
-            while (ahead.valid(a) && !*abort_flag) {
+            while (!a.stall && ahead.valid(a) && !*abort_flag) {
                 // refilling a stage: wait until all consumer warps released it
-                if (round > 0 && !mbar_wait_bounded(empty0 + 8u * pst,
-                                                    (uint32_t)((round - 1) & 1), abort_flag)) {
+                if (round > 0 && !mbar_wait_bounded(empty0 + 8u * pst, (uint32_t)((round - 1) & 1),
+                                                    abort_flag, a.wait_ns)) {
                     *abort_flag = 1;
                     atomicOr(a.status, 1);
                     break;
@@ -940,7 +958,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
             }
             // Every copy must have landed before the CTA (and its shared
             // memory) goes away; the consumers wait for all of them unless a
-            // wait was abandoned, so this only waits in that case.
+            // wait was abandoned, so this only waits in that case, and always
+            // with the full limit whatever wait_ns is.
             const int zero = 0;
             for (int s = 0; s < a.stages; ++s)
                 if (issues[s] > 0)
@@ -959,7 +978,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
                 for (int q = q0; q < q1 && e < kMaxEvents; q += a.CS - cb, ++rb, cb = 0) {
                     const int seg_n = q1 - q < a.CS - cb ? q1 - q : a.CS - cb;
                     if (cb == 0 && seg_n == a.CS) continue;  // whole row block: stored directly
-                    if (!mbar_wait_bounded(seg_done0 + 8u * e, 0, abort_flag)) {
+                    if (!mbar_wait_bounded(seg_done0 + 8u * e, 0, abort_flag, a.wait_ns)) {
                         *abort_flag = 1;
                         atomicOr(a.status, 1);
                         return;
@@ -1022,7 +1041,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
         for (int q = q0; q < q1; q += a.CS - cb, ++rb, cb = 0) {
             const int seg_n = q1 - q < a.CS - cb ? q1 - q : a.CS - cb;
             for (int k = 0; k < seg_n; ++k) {
-                if (ok && !mbar_wait_bounded(full0 + 8u * st, ph, abort_flag)) {
+                if (ok && !mbar_wait_bounded(full0 + 8u * st, ph, abort_flag, a.wait_ns)) {
                     ok = false;
                     *abort_flag = 1;
                     atomicOr(a.status, 1);
@@ -1090,7 +1109,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
 }
 
 int device_sm_count() {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
         cudaGetLastError();
@@ -1107,13 +1126,32 @@ int device_sm_count() {
     return cache[dev];
 }
 
-size_t gemv_scratch_bytes(int streams, int M, int N, int K, int num_sms) {
+size_t gemv_partial_bytes(int streams, int M, int N, int K, int num_sms) {
     return make_plan(streams, M, N, K, num_sms).total;
+}
+
+size_t gemv_counter_bytes(int N) {
+    return (size_t)ceil_div((long long)geometry(N, kChunkK).RB * kBlockTiles * 4, 256) * 256;
+}
+
+bool gemv_plan_aligned(int streams, int M, int N, int K, int num_sms) {
+    return plan_aligned(make_plan(streams, M, N, K, num_sms));
+}
+
+namespace {
+std::atomic<int> g_test_stall{0};
+std::atomic<unsigned long long> g_test_wait_ns{kWaitLimitNs};
+}  // namespace
+
+void set_test_stall(int stall, unsigned long long wait_ns) {
+    g_test_wait_ns.store(wait_ns);
+    g_test_stall.store(stall);
 }
 
 template <int NS, int NT, bool ONE, bool DIAG, bool EM>
 static cudaError_t launch_t(const Plan& p, const KArgs& a, cudaStream_t s) {
-    static bool attr_done[64] = {false};
+    // set once per device; a second thread racing here sets it again, harmlessly
+    static std::atomic<bool> attr_done[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
@@ -1139,16 +1177,16 @@ static cudaError_t launch_t(const Plan& p, const KArgs& a, cudaStream_t s) {
 
 cudaError_t launch_stream_gemv(int streams, const void* x, int M, int K, const void* packed, int N,
                                float scale_a, float scale_b, int act, void* out, int* status,
-                               void* scratch, size_t scratch_bytes, int num_sms, bool early_weights,
-                               cudaStream_t s) {
+                               int* counters, void* partials, size_t partial_bytes, int num_sms,
+                               bool early_weights, cudaStream_t s) {
     const Plan p = make_plan(streams, M, N, K, num_sms);
-    if (scratch_bytes < p.total) return cudaErrorInvalidValue;
+    if (partial_bytes < p.total || !plan_aligned(p)) return cudaErrorInvalidValue;
     KArgs a;
     a.x = reinterpret_cast<const __nv_bfloat16*>(x);
     a.blob = reinterpret_cast<const uint8_t*>(packed);
     a.out = reinterpret_cast<__nv_bfloat16*>(out);
-    a.counters = reinterpret_cast<int*>(reinterpret_cast<char*>(scratch) + p.counters_off);
-    a.partials = reinterpret_cast<float*>(reinterpret_cast<char*>(scratch) + p.partials_off);
+    a.counters = counters;
+    a.partials = reinterpret_cast<float*>(partials);
     a.status = status;
     a.L = p.L;
     a.M = M;
@@ -1172,6 +1210,8 @@ cudaError_t launch_stream_gemv(int streams, const void* x, int M, int K, const v
     a.scale_b = scale_b;
     a.act = act;
     a.early_weights = early_weights ? 1 : 0;
+    a.wait_ns = g_test_wait_ns.load();
+    a.stall = g_test_stall.load();
     a.fast = (unsigned long long)p.L * (unsigned long long)p.R < (1ull << 32) ? 1 : 0;
     a.div_R = FastDiv::make((unsigned)p.R);
     a.div_L = FastDiv::make((unsigned)(p.L < (1LL << 32) ? p.L : 1));

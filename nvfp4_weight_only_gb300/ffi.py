@@ -30,10 +30,13 @@ EXPORTS = [
     "nvfp4_quantize_scratch_bytes", "nvfp4_quantize", "nvfp4_repacked_bytes", "nvfp4_repack",
     "nvfp4_repacked_gate_up_bytes", "nvfp4_repack_gate_up", "nvfp4_unpack",
     "nvfp4_gemv_workspace_bytes", "nvfp4_gemv", "ffn_swiglu_nvfp4_workspace_bytes",
+    "ffn_swiglu_nvfp4_hidden_offset",
     "ffn_swiglu_nvfp4", "ffn_gate_up_nvfp4_workspace_bytes", "ffn_gate_up_nvfp4",
-    "ffn_swiglu_nvfp4_noalloc",
+    "ffn_swiglu_nvfp4_noalloc", "nvfp4_noalloc_status",
     "nvfp4_workspace_init", "nvfp4_workspace_status", "nvfp4_status_string",
 ]
+# Every symbol declared in include/nvfp4ffn_testing.h (test hooks).
+TESTING_EXPORTS = ["nvfp4_testing_inject_stall", "nvfp4_testing_plan_aligned"]
 
 
 class Nvfp4Error(RuntimeError):
@@ -70,10 +73,14 @@ def load(build_if_missing: bool = False):
         "nvfp4_gemv_workspace_bytes": (sz, [i32, i32, i32]),
         "nvfp4_gemv": (i32, [vp, i32, i32, vp, f32, i32, vp, vp, sz, vp]),
         "ffn_swiglu_nvfp4_workspace_bytes": (sz, [i32, i32, i32]),
+        "ffn_swiglu_nvfp4_hidden_offset": (sz, []),
         "ffn_swiglu_nvfp4": (i32, [vp, i32, i32, i32, vp, f32, f32, vp, f32, i32, vp, vp, sz, vp]),
         "ffn_gate_up_nvfp4_workspace_bytes": (sz, [i32, i32, i32]),
         "ffn_gate_up_nvfp4": (i32, [vp, i32, i32, i32, vp, f32, f32, i32, vp, vp, sz, vp]),
         "ffn_swiglu_nvfp4_noalloc": (i32, [vp, i32, i32, i32, vp, f32, f32, vp, f32, i32, vp, vp]),
+        "nvfp4_noalloc_status": (i32, [vp]),
+        "nvfp4_testing_inject_stall": (i32, [i32, ctypes.c_ulonglong]),
+        "nvfp4_testing_plan_aligned": (i32, [i32, i32, i32, i32, i32]),
         "nvfp4_workspace_init": (i32, [vp, sz, vp]),
         "nvfp4_workspace_status": (i32, [vp, vp]),
         "nvfp4_status_string": (ctypes.c_char_p, [i32]),
@@ -263,9 +270,9 @@ def ffn_gate_up_nvfp4(x: torch.Tensor, gate_up_packed: torch.Tensor, gate_scale2
 
 
 def ffn_hidden_view(ws: torch.Tensor, M: int, I: int) -> torch.Tensor:
-    """The bf16 activation h [M, I] that ffn_swiglu_nvfp4 leaves in its workspace
-    (it starts right after the 256-byte status area)."""
-    return ws[256:256 + M * I * 2].view(torch.bfloat16).view(M, I)
+    """The bf16 activation h [M, I] that ffn_swiglu_nvfp4 leaves in its workspace."""
+    off = load().ffn_swiglu_nvfp4_hidden_offset()
+    return ws[off:off + M * I * 2].view(torch.bfloat16).view(M, I)
 
 
 def nvfp4_workspace_init(ws: torch.Tensor) -> None:
@@ -276,3 +283,9 @@ def nvfp4_workspace_init(ws: torch.Tensor) -> None:
 def nvfp4_workspace_status(ws: torch.Tensor) -> int:
     """Synchronise, read and clear the device status word (0 = OK, 7 = timeout)."""
     return load().nvfp4_workspace_status(_ptr(ws), _stream(ws.device))
+
+
+def nvfp4_noalloc_status(device=None) -> int:
+    """Status of the fixed-workspace FFN calls (0 = OK, 7 = timeout, after which
+    the library has zero-filled its array again)."""
+    return load().nvfp4_noalloc_status(_stream(device))

@@ -9,7 +9,8 @@ import pytest
 from nvfp4_weight_only_gb300 import ffi
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "nvfp4ffn.h")
+INCLUDE = os.path.join(ROOT, "include")
+HEADERS = sorted(os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h"))
 
 
 @pytest.fixture(scope="module")
@@ -18,13 +19,16 @@ def lib():
 
 
 def header_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
 
 
 def test_header_declares_the_binding_exports():
-    assert header_functions() == sorted(ffi.EXPORTS)
+    assert len(HEADERS) == 2
+    assert header_functions() == sorted(ffi.EXPORTS + ffi.TESTING_EXPORTS)
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -112,3 +116,42 @@ def test_binding_raises_without_cuda_tensors():
     with pytest.raises(ValueError):
         ffi.nvfp4_gemv(torch.zeros(1, 64, dtype=torch.bfloat16), torch.zeros(10, dtype=torch.uint8),
                        1.0, 64)
+
+
+def test_shared_memory_plans_are_aligned(lib):
+    """Every shared-memory plan the GEMV kernel can be launched with keeps the
+    alignment its accesses assume (bulk-copy stages and vector loads on 16
+    bytes, mbarriers on 8, the misc area on 128) and fits the per-block limit,
+    for every M, odd stage counts included, across SM counts and shapes."""
+    shapes = [(5120, 17408), (17408, 5120), (4096, 12288), (12288, 4096), (5376, 21504),
+              (21504, 5376), (65536, 21504), (65536, 4096), (4096, 4096), (200, 272), (16, 16),
+              (1, 2048), (300, 21504), (384, 1024)]
+    for streams in (1, 2):
+        for M in range(1, 17):
+            for N, K in shapes:
+                for sms in (152, 148, 132, 160, 7, 1):
+                    assert lib.nvfp4_testing_plan_aligned(streams, M, N, K, sms) == 1, \
+                        (streams, M, N, K, sms)
+    assert lib.nvfp4_testing_plan_aligned(3, 1, 256, 256, 152) == -1
+    assert lib.nvfp4_testing_plan_aligned(1, 17, 256, 256, 152) == -1
+
+
+def test_testing_stall_switch_validates_its_limit(lib):
+    assert lib.nvfp4_testing_inject_stall(1, 10) == 4          # below 1 us: NVFP4_ERR_RANGE
+    assert lib.nvfp4_testing_inject_stall(1, 2 * 10 ** 9) == 4  # above 1 s
+    assert lib.nvfp4_testing_inject_stall(0, 0) == 0           # off: always accepted
+
+
+def test_noalloc_validation_touches_nothing(lib):
+    """Argument errors of the fixed-workspace FFN are found on the host before
+    any device set-up (these calls run without a GPU)."""
+    f = lib.ffn_swiglu_nvfp4_noalloc
+    A = [ctypes.c_void_p(0x10000 * i) for i in range(1, 5)]
+    assert f(NULL, 1, 256, 512, A[1], 1.0, 1.0, A[2], 1.0, 0, A[3], S) == 1
+    assert f(A[0], 17, 256, 512, A[1], 1.0, 1.0, A[2], 1.0, 0, A[3], S) == 4
+    assert f(A[0], 1, 256, 512, A[1], 1.0, 1.0, A[2], 1.0, 7, A[3], S) == 4
+    assert f(A[0], 1, 250, 512, A[1], 1.0, 1.0, A[2], 1.0, 0, A[3], S) == 2
+    assert f(A[0], 1, 256, 512, A[1], 1.0, 1.0, A[2], 1.0, 0, MISALIGNED, S) == 3
+    assert f(A[0], 1, 256, 512, A[1], 1.0, 1.0, A[2], 1.0, 0, A[0], S) == 8
+    B = [ctypes.c_void_p(0x10000000 * i) for i in range(1, 5)]  # disjoint at this size
+    assert f(B[0], 16, 8192, 32768, B[1], 1.0, 1.0, B[2], 1.0, 0, B[3], S) == 5
