@@ -31,6 +31,7 @@
 #include <cuda_bf16.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "device_util.cuh"
 #include "internal.h"
@@ -264,7 +265,7 @@ struct StepCursor {
 // Not inlined: the last range's epilogue runs it for several elements per lane
 // right after the stream, and one shared copy of its code costs one round of
 // instruction fetch misses instead of one per unrolled element.
-__device__ __noinline__ __nv_bfloat16 gated_product(int act, float g, float u) {
+__device__ __forceinline__ __nv_bfloat16 gated_product_inline(int act, float g, float u) {
     const float y = (act == 0) ? g : 1.5957691216057308f * (g + 0.044715f * g * g * g);
     if (y < 0.0f) {
         const float e = expf(y);
@@ -277,6 +278,10 @@ __device__ __noinline__ __nv_bfloat16 gated_product(int act, float g, float u) {
         if ((bits & 0xFFFFu) == 0x8000u) return __ushort_as_bfloat16((unsigned short)(bits >> 16));
     }
     return __float2bfloat16_rn(p);
+}
+
+__device__ __noinline__ __nv_bfloat16 gated_product(int act, float g, float u) {
+    return gated_product_inline(act, g, u);
 }
 
 template <int NS>
@@ -747,22 +752,18 @@ __device__ __forceinline__ constexpr bool kScaleInA() {
 // a zero accumulator, and the two row scales (E4M3 -> f16 -> f32, exact) are
 // applied to those fp32 block sums with FFMAs.  Every MMA is independent; the
 // FMA pipe takes the scaling, which leaves the ALU pipe to the decode.
+// wl: this lane's 16 code bytes of the chunk's unit; sl: the scale bytes of
+// its row pair (g, g+8); xl[nt]: its B fragments of token tile nt (32 bytes).
+// The second stream's unit follows the first's (gate/up interleave).
 template <int NS, int NT, bool ONE>
-__device__ __forceinline__ void process_chunk(const uint8_t* stage, const uint8_t* xs,
-                                              int x_stride, int M, int j, int cj, int warp,
-                                              int lane, float (&acc)[NS][NT][4]) {
-    constexpr int UB = kUnitBytes * NS;
-    const int g = lane >> 2, tq = lane & 3;
+__device__ __forceinline__ void process_chunk(const uint8_t* wl, const uint8_t* sl,
+                                              const uint8_t* const (&xl)[NT],
+                                              float (&acc)[NS][NT][4]) {
     uint32_t b[NT][8];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        // B column (token row of x) this lane supplies.  Columns past the last
-        // token repeat its row: their sums land in output columns that are
-        // never stored, and every load stays inside the staged rows.
-        const int token = min(nt * 8 + g, M - 1);
-        const uint8_t* px = xs + token * x_stride + cj * 128 + tq * 32;
-        const uint4 v0 = *reinterpret_cast<const uint4*>(px);
-        const uint4 v1 = *reinterpret_cast<const uint4*>(px + 16);
+        const uint4 v0 = *reinterpret_cast<const uint4*>(xl[nt]);
+        const uint4 v1 = *reinterpret_cast<const uint4*>(xl[nt] + 16);
         b[nt][0] = v0.x;
         b[nt][1] = v0.y;
         b[nt][2] = v0.z;
@@ -772,12 +773,10 @@ __device__ __forceinline__ void process_chunk(const uint8_t* stage, const uint8_
         b[nt][6] = v1.z;
         b[nt][7] = v1.w;
     }
-    const uint8_t* unit = stage + (j * kBlockTiles + warp) * UB;
 #pragma unroll
     for (int si = 0; si < NS; ++si) {
-        const uint4 cw = *reinterpret_cast<const uint4*>(unit + si * kUnitBytes + lane * 16);
-        const uint2 sw =
-            *reinterpret_cast<const uint2*>(unit + si * kUnitBytes + kUnitCodeBytes + g * 8);
+        const uint4 cw = *reinterpret_cast<const uint4*>(wl + si * kUnitBytes);
+        const uint2 sw = *reinterpret_cast<const uint2*>(sl + si * kUnitBytes);
         const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
         for (int jb = 0; jb < 4; ++jb) {
@@ -823,21 +822,19 @@ __device__ __forceinline__ void process_chunk(const uint8_t* stage, const uint8_
 // block j's sums for tokens 0, 1; lane quarter t then applies block t's two
 // row scales (rows g, g+8) with FFMAs.  Per k16 block: 4 cvt + 1 MMA; per
 // chunk and lane: one scale-pair select and conversion and 2 (ONE) or 4 FFMAs.
+// wl, sl as for process_chunk; xl: this lane's 16 bytes of the chunk's first
+// 512-byte half of the diagonal token area (the second half follows).
 template <int NS, bool ONE>
-__device__ __forceinline__ void process_chunk_diag(const uint8_t* stage, const uint8_t* xs, int j,
-                                                   int cj, int warp, int lane, uint32_t scale_sel,
+__device__ __forceinline__ void process_chunk_diag(const uint8_t* wl, const uint8_t* sl,
+                                                   const uint8_t* xl, uint32_t scale_sel,
                                                    float (&acc)[NS][1][4]) {
-    constexpr int UB = kUnitBytes * NS;
-    const int g = lane >> 2;
-    const uint4 v0 = *reinterpret_cast<const uint4*>(xs + cj * 1024 + lane * 16);
-    const uint4 v1 = *reinterpret_cast<const uint4*>(xs + cj * 1024 + 512 + lane * 16);
+    const uint4 v0 = *reinterpret_cast<const uint4*>(xl);
+    const uint4 v1 = *reinterpret_cast<const uint4*>(xl + 512);
     const uint32_t b[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    const uint8_t* unit = stage + (j * kBlockTiles + warp) * UB;
 #pragma unroll
     for (int si = 0; si < NS; ++si) {
-        const uint4 cw = *reinterpret_cast<const uint4*>(unit + si * kUnitBytes + lane * 16);
-        const uint2 sw =
-            *reinterpret_cast<const uint2*>(unit + si * kUnitBytes + kUnitCodeBytes + g * 8);
+        const uint4 cw = *reinterpret_cast<const uint4*>(wl + si * kUnitBytes);
+        const uint2 sw = *reinterpret_cast<const uint2*>(sl + si * kUnitBytes);
         const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
         float d[4];
 #pragma unroll
@@ -885,6 +882,76 @@ __device__ __forceinline__ void issue_step(const KArgs& a, const StepCursor& cur
     ++issues[st];
 }
 
+// The row blocks (and counter values) a warp must still resolve, oldest
+// first, up to four.  PendRegs keeps them in registers with compile-time
+// indexing (a dynamically indexed array lives in local memory, whose L1 share
+// is small next to the shared-memory carve-out); PendArray is the plain array.
+// Measured: the registers win for the diagonal layout (M <= 2), the array for
+// the others, whose register budget the scalars crowd.
+struct PendRegs {
+    int rb0 = 0, rb1 = 0, rb2 = 0, rb3 = 0, o0 = 0, o1 = 0, o2 = 0, o3 = 0;
+    __device__ __forceinline__ void set(int n, int rb, int old) {
+        rb0 = n == 0 ? rb : rb0;
+        rb1 = n == 1 ? rb : rb1;
+        rb2 = n == 2 ? rb : rb2;
+        rb3 = n == 3 ? rb : rb3;
+        o0 = n == 0 ? old : o0;
+        o1 = n == 1 ? old : o1;
+        o2 = n == 2 ? old : o2;
+        o3 = n == 3 ? old : o3;
+    }
+    __device__ __forceinline__ void pop_front() {
+        rb0 = rb1;
+        rb1 = rb2;
+        rb2 = rb3;
+        o0 = o1;
+        o1 = o2;
+        o2 = o3;
+    }
+    template <int I>
+    __device__ __forceinline__ int rb() const {
+        return I == 0 ? rb0 : I == 1 ? rb1 : I == 2 ? rb2 : rb3;
+    }
+    template <int I>
+    __device__ __forceinline__ int old() const {
+        return I == 0 ? o0 : I == 1 ? o1 : I == 2 ? o2 : o3;
+    }
+};
+
+struct PendArray {
+    int rb_[4], o_[4];
+    __device__ __forceinline__ void set(int n, int rb, int old) {
+        rb_[n] = rb;
+        o_[n] = old;
+    }
+    __device__ __forceinline__ void pop_front() {
+        for (int i = 1; i < 4; ++i) {
+            rb_[i - 1] = rb_[i];
+            o_[i - 1] = o_[i];
+        }
+    }
+    template <int I>
+    __device__ __forceinline__ int rb() const {
+        return rb_[I];
+    }
+    template <int I>
+    __device__ __forceinline__ int old() const {
+        return o_[I];
+    }
+};
+
+// A consumer's wait on a stage that was not full at the first test: bounded,
+// and kept out of line so that the step loop stays small.  On giving up it
+// raises the CTA's abort flag and the device status word.
+__device__ __noinline__ bool wait_stage_slow(uint32_t bar, uint32_t parity,
+                                             volatile int* abort_flag, unsigned long long limit_ns,
+                                             int* status) {
+    if (mbar_wait_bounded(bar, parity, abort_flag, limit_ns)) return true;
+    *abort_flag = 1;
+    atomicOr(status, 1);
+    return false;
+}
+
 // ONE: a single token row (M == 1), which needs only the even MMA columns.
 // DIAG: M <= 2 with the diagonal token layout (stage_x_diag).
 // EM: element-major split-K partials (M <= kElemMajorMaxM).
@@ -913,7 +980,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
             mbar_init(full0 + 8u * s, 1);
-            mbar_init(empty0 + 8u * s, kWarps);
+            mbar_init(empty0 + 8u * s, kConsumerThreads);  // every consumer lane arrives
             issues[s] = 0;
         }
         for (int e = 0; e < kMaxEvents; ++e) {
@@ -996,35 +1063,43 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
     }
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    float acc[NS][NT][4], hi[NS][NT][4], lo[NS][NT][4];
-#pragma unroll
-    for (int si = 0; si < NS; ++si)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                acc[si][nt][e] = 0.0f;
-                hi[si][nt][e] = 0.0f;
-                lo[si][nt][e] = 0.0f;
-            }
-    int st = 0;
-    uint32_t ph = 0;
+    // The ring as seen by this lane: the offset of the current stage, its
+    // "full" barrier (its "empty" barrier lies bar_gap further) and phase, and
+    // the lane's code and scale addresses in stage 0.
+    constexpr int UB = kUnitBytes * NS;
+    const uint8_t* const wl0 = smem + warp * UB + lane * 16;
+    const uint8_t* const sl0 = smem + warp * UB + kUnitCodeBytes + (lane >> 2) * 8;
+    const uint32_t stage_bytes = (uint32_t)a.stage_bytes;
+    const uint32_t ring_bytes = stage_bytes * (uint32_t)a.stages;
+    const uint32_t bar_gap = empty0 - full0;
+    uint32_t st_off = 0, bar_f = full0, ph = 0;
     bool ok = true;
     // row blocks whose tile this warp must still reduce (it arrived last)
     constexpr int kMaxPending = 4;
-    int pending[kMaxPending], pending_old[kMaxPending];
+    static_assert(kMaxPending == 4, "the pending FIFO holds four entries");
+    using Pend = typename std::conditional<DIAG, PendRegs, PendArray>::type;
+    Pend pend;
     int n_pending = 0;
     int evt = 0;  // partial segments so far (publisher events)
     constexpr int kFoldSteps = kFoldChunks / CPS;  // steps between folds
-    static_assert(kFoldSteps * CPS == kFoldChunks && (kFoldSteps & (kFoldSteps - 1)) == 0,
-                  "fold period is a power-of-two number of steps");
+    static_assert(kFoldSteps * CPS == kFoldChunks, "fold period is a whole number of steps");
+    // Token fragments: this lane's bytes of chunk 0 of the staged rows, and
+    // the distance between consecutive chunks.
+    constexpr int kXChunk = DIAG ? 1024 : 128;
+    const uint8_t* xl0[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int token = min(nt * 8 + (lane >> 2), a.M - 1);
+        xl0[nt] = DIAG ? xs + lane * 16 : xs + token * a.x_stride + tq * 32;
+    }
+    const int C = a.C;
     for (int r = blockIdx.x; r < a.R; r += a.grid) {
         // ---- a new range: steps q0 .. q1-1; stage its token rows
         const int q0 = (int)range_start(a, r), q1 = (int)range_start(a, r + 1);
         int rb = rb_of_step(a, q0);
         int cb = q0 - rb * a.CS;
         const int c_start = cb * CPS;
-        const int nx = (q1 - q0) * CPS < a.C ? (q1 - q0) * CPS : a.C;
+        const int nx = (q1 - q0) * CPS < C ? (q1 - q0) * CPS : C;
         consumer_sync();  // every warp is done with the previous range's x
         if (DIAG)
             stage_x_diag(a, xs, c_start, nx, tok_unscale, amax_u);
@@ -1036,48 +1111,71 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
 #pragma unroll
             for (int e = 0; e < 2; ++e)
                 unscale[nt][e] = tok_unscale[DIAG ? e : nt * 8 + 2 * tq + e];
-        int ci = 0;
+        // the range's sums (every segment leaves them at zero again)
+        float acc[NS][NT][4], hi[NS][NT][4], lo[NS][NT][4];
+#pragma unroll
+        for (int si = 0; si < NS; ++si)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc[si][nt][e] = 0.0f;
+                    hi[si][nt][e] = 0.0f;
+                    lo[si][nt][e] = 0.0f;
+                }
+        int ci = 0;  // staged chunk of the current step
         // ---- the range's segments: the run of its steps inside one row block
         for (int q = q0; q < q1; q += a.CS - cb, ++rb, cb = 0) {
             const int seg_n = q1 - q < a.CS - cb ? q1 - q : a.CS - cb;
-            for (int k = 0; k < seg_n; ++k) {
-                if (ok && !mbar_wait_bounded(full0 + 8u * st, ph, abort_flag, a.wait_ns)) {
-                    ok = false;
-                    *abort_flag = 1;
-                    atomicOr(a.status, 1);
-                }
-                if (ok) {
-                    const uint8_t* stage = smem + (size_t)st * a.stage_bytes;
+            // the steps in groups of kFoldSteps, the sums folded after each
+#pragma unroll 1
+            for (int k0 = 0; k0 < seg_n; k0 += kFoldSteps) {
+                const int kn = seg_n - k0 < kFoldSteps ? seg_n - k0 : kFoldSteps;
+#pragma unroll 1
+                for (int k = 0; k < kn; ++k) {
+                    // A warp that gave up a wait keeps walking the steps (every
+                    // consumer warp must reach each range's barriers) but waits
+                    // no more; its results are discarded.
+                    if (!mbar_try_wait(bar_f, ph) && ok)
+                        ok = wait_stage_slow(bar_f, ph, abort_flag, a.wait_ns, a.status);
+                    const uint8_t* wl = wl0 + st_off;
+                    const uint8_t* sl = sl0 + st_off;
+                    const int xo = ci * kXChunk;
 #pragma unroll
                     for (int j = 0; j < CPS; ++j) {
-                        if constexpr (DIAG)
-                            process_chunk_diag<NS, ONE>(stage, xs, j, ci + j, warp, lane,
-                                                        scale_sel, acc);
-                        else
-                            process_chunk<NS, NT, ONE>(stage, xs, a.x_stride, a.M, j, ci + j,
-                                                       warp, lane, acc);
+                        if constexpr (DIAG) {
+                            process_chunk_diag<NS, ONE>(wl + j * kBlockTiles * UB,
+                                                        sl + j * kBlockTiles * UB,
+                                                        xl0[0] + xo + j * kXChunk, scale_sel, acc);
+                        } else {
+                            const uint8_t* xj[NT];
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) xj[nt] = xl0[nt] + xo + j * kXChunk;
+                            process_chunk<NS, NT, ONE>(wl + j * kBlockTiles * UB,
+                                                       sl + j * kBlockTiles * UB, xj, acc);
+                        }
                     }
+                    // Release the stage to the producer (each lane for itself).
+                    mbar_arrive(bar_f + bar_gap);
+                    st_off += stage_bytes;
+                    bar_f += 8u;
+                    if (st_off == ring_bytes) {
+                        st_off = 0;
+                        bar_f = full0;
+                        ph ^= 1u;
+                    }
+                    ci += CPS;
+                    if (ci >= C) ci -= C;
                 }
-                // Release the stage to the producer.
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty0 + 8u * st);
-                if (++st == a.stages) {
-                    st = 0;
-                    ph ^= 1u;
-                }
-                ci += CPS;
-                if (ci >= a.C) ci -= a.C;
-                if ((k & (kFoldSteps - 1)) == kFoldSteps - 1 || k == seg_n - 1) {
 #pragma unroll
-                    for (int si = 0; si < NS; ++si)
+                for (int si = 0; si < NS; ++si)
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
+                    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                            for (int e = 0; e < 4; e += ONE ? 2 : 1) {
-                                two_sum_acc(hi[si][nt][e], lo[si][nt][e], acc[si][nt][e]);
-                                acc[si][nt][e] = 0.0f;
-                            }
-                }
+                        for (int e = 0; e < 4; e += ONE ? 2 : 1) {
+                            two_sum_acc(hi[si][nt][e], lo[si][nt][e], acc[si][nt][e]);
+                            acc[si][nt][e] = 0.0f;
+                        }
             }
             const int old = finish_segment<NS, NT, DIAG, EM>(a, hi, lo, unscale, r, q0, rb,
                                                              cb + seg_n - 1, warp, lane, ok, evt,
@@ -1085,27 +1183,27 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
             if (old != -1) {
                 ++evt;
                 if (n_pending == kMaxPending) {  // resolve the oldest now
-                    const int o = pending_old_value(a, pending_old[0], warp, pub_done0, pub_old,
-                                                    abort_flag);
-                    if (resolve_tile(a, pending[0], warp, lane, o))
-                        reduce_any<NS, NT, DIAG, EM>(a, pending[0], warp, lane, ok);
-                    for (int i = 1; i < kMaxPending; ++i) {
-                        pending[i - 1] = pending[i];
-                        pending_old[i - 1] = pending_old[i];
-                    }
+                    const int o = pending_old_value(a, pend.template old<0>(), warp, pub_done0,
+                                                    pub_old, abort_flag);
+                    if (resolve_tile(a, pend.template rb<0>(), warp, lane, o))
+                        reduce_any<NS, NT, DIAG, EM>(a, pend.template rb<0>(), warp, lane, ok);
+                    pend.pop_front();
                     --n_pending;
                 }
-                pending[n_pending] = rb;
-                pending_old[n_pending] = old;
+                pend.set(n_pending, rb, old);
                 ++n_pending;
             }
         }
     }
-    for (int i = 0; i < n_pending; ++i) {
-        const int o = pending_old_value(a, pending_old[i], warp, pub_done0, pub_old, abort_flag);
-        if (resolve_tile(a, pending[i], warp, lane, o))
-            reduce_any<NS, NT, DIAG, EM>(a, pending[i], warp, lane, ok);
-    }
+    // resolve what is still pending, oldest first
+    auto resolve = [&](int rbv, int oldv) {
+        const int o = pending_old_value(a, oldv, warp, pub_done0, pub_old, abort_flag);
+        if (resolve_tile(a, rbv, warp, lane, o)) reduce_any<NS, NT, DIAG, EM>(a, rbv, warp, lane, ok);
+    };
+    if (n_pending > 0) resolve(pend.template rb<0>(), pend.template old<0>());
+    if (n_pending > 1) resolve(pend.template rb<1>(), pend.template old<1>());
+    if (n_pending > 2) resolve(pend.template rb<2>(), pend.template old<2>());
+    if (n_pending > 3) resolve(pend.template rb<3>(), pend.template old<3>());
 }
 
 int device_sm_count() {
