@@ -468,6 +468,35 @@ def run_sweep(args, ffi, synth, dev, timer, sampler, layers, H, I, peak):
         for act, name in ((0, "silu"), (1, "gelu_tanh")):
             bm[f"M{M}_{name}"] = ffn_case(layers, H, I, M, act, 0.01)
     res[f"ffn_{H}x{I}_outliers_1pct"] = bm
+    # LoRA overlay (rank 16 on gate, up and down; one adapter shared by the layers)
+    lr = {}
+    r = 16
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(17)
+
+    def rnd(*shape):
+        return (torch.randn(shape, generator=gen, device=dev) * 0.05).to(torch.bfloat16)
+
+    pairs = dict(gate=(rnd(r, H), rnd(I, r)), up=(rnd(r, H), rnd(I, r)), down=(rnd(r, I), rnd(H, r)))
+    for M in (1, 8):
+        x = synth.activations_bf16(M, H, seed=M, device=dev)
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        ws = ffi.workspace(ffi.load().ffn_swiglu_nvfp4_lora_workspace_bytes(M, H, I, r), dev)
+
+        def fn():
+            for (gu, g2, u2, dn, d2) in layers:
+                ffi.ffn_swiglu_nvfp4_lora(x, gu, g2, u2, dn, d2, I, 0, ws=ws, out=out, **pairs)
+
+        g = timer.capture(fn)
+        w0 = time.time()
+        t = timer.time(g, reps, warmup=3) / (reps * len(layers))
+        sampler.mark(w0, time.time())
+        launches += 6 * len(layers) * reps
+        lr[f"M{M}_r{r}"] = _layer_entry(t, H, I, M, peak)
+        if ffi.nvfp4_workspace_status(ws) != 0:
+            raise RuntimeError("device status word reports a bounded wait abandoned")
+        del g
+    res[f"ffn_{H}x{I}_lora_gate_up_down"] = lr
     torch.cuda.empty_cache()
 
     for key, Hs, Is, Ls, Ms in (("spec_verify", 4096, 12288, 32, (2, 3)),

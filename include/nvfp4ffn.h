@@ -196,6 +196,53 @@ nvfp4_status ffn_gate_up_nvfp4(const void* x, int M, int H, int I, const void* g
                                float gate_scale2, float up_scale2, nvfp4_act act, void* h,
                                void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* ------------------------------------------------------------------ LoRA overlay */
+
+/*
+ * The adapter overlay of the dense-FFN page (DenseFfnLayer::apply_lora_gate_up
+ * and apply_lora_down): gate and up take dW x after their projections and
+ * before the activation, the output takes dW h after the down projection,
+ * contracted over the activation h.  dW = B A with A [r, in] and B [out, r]
+ * bf16 row-major (device), 1 <= r <= 64; any alpha/r is folded into B.  Each
+ * intermediate is bf16: xa = bf16(A v), d = bf16(B xa), base = bf16(base + d).
+ */
+
+/* Workspace bytes for ffn_swiglu_nvfp4_lora (the FFN's plus the adapter
+ * intermediates); contract as for nvfp4_gemv. */
+size_t ffn_swiglu_nvfp4_lora_workspace_bytes(int M, int H, int I, int rank);
+
+/*
+ * ffn_swiglu_nvfp4 with the overlay:
+ *   g = bf16(bf16(gate_scale2 * gate.x) + bf16(Bg bf16(Ag x)))   (likewise u)
+ *   h = bf16(act(g) * u),  out = bf16(bf16(down_scale2 * down.h) + bf16(Bd bf16(Ad h)))
+ * gate_a [r, H] / gate_b [I, r], up_a [r, H] / up_b [I, r], down_a [r, I] /
+ * down_b [H, r] (device, bf16); a pair given as two NULL pointers is absent
+ * (its delta is zero).  A pair with one NULL pointer is NVFP4_ERR_NULL; rank
+ * outside [1, 64] is NVFP4_ERR_RANGE.  Other arguments and requirements as
+ * ffn_swiglu_nvfp4.  Up to four small launches join the FFN's two.
+ */
+nvfp4_status ffn_swiglu_nvfp4_lora(const void* x, int M, int H, int I,
+                                   const void* gate_up_packed, float gate_scale2,
+                                   float up_scale2, const void* down_packed,
+                                   float down_scale2, nvfp4_act act, int rank,
+                                   const void* gate_a, const void* gate_b, const void* up_a,
+                                   const void* up_b, const void* down_a, const void* down_b,
+                                   void* out, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Scratch bytes for nvfp4_lora_apply (the bf16 xa [M, r]). */
+size_t nvfp4_lora_apply_scratch_bytes(int M, int rank);
+
+/*
+ * The page's apply_lora_delta on its own: base[m][n] = bf16(base[m][n] +
+ * bf16(sum_j b[n][j] xa[m][j])) with xa = bf16(a v):  v (device) bf16 [M, K],
+ * a [rank, K], b [N, rank] (device, bf16), base (device, in/out) bf16 [M, N],
+ * scratch (device) >= nvfp4_lora_apply_scratch_bytes.  1 <= M <= 16, K even,
+ * v and base disjoint.
+ */
+nvfp4_status nvfp4_lora_apply(const void* v, int M, int K, const void* a, const void* b,
+                              int rank, int N, void* base, void* scratch, size_t scratch_bytes,
+                              cudaStream_t stream);
+
 /*
  * ffn_swiglu_nvfp4 for callers that cannot allocate device memory where they
  * run the FFN (a process that reserves the device's memory for its own pool at

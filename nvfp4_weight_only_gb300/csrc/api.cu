@@ -206,6 +206,123 @@ nvfp4_status ffn_swiglu_nvfp4(const void* x, int M, int H, int I, const void* ga
     return cuda_status(e);
 }
 
+// LoRA FFN workspace: the FFN's, then xa_gate [M, r], xa_up [M, r], the gate
+// and up deltas [M, I] each, and xa_down [M, r] (all bf16).
+struct LoraLayout {
+    FfnLayout ffn;
+    size_t xa_g, xa_u, d_g, d_u, xa_d, total;
+};
+
+LoraLayout lora_layout(int M, int H, int I, int r, int sms) {
+    LoraLayout l;
+    l.ffn = ffn_layout(M, H, I, sms);
+    const size_t xr = round256((size_t)M * r * 2), xi = round256((size_t)M * I * 2);
+    l.xa_g = l.ffn.total;
+    l.xa_u = l.xa_g + xr;
+    l.d_g = l.xa_u + xr;
+    l.d_u = l.d_g + xi;
+    l.xa_d = l.d_u + xi;
+    l.total = l.xa_d + xr;
+    return l;
+}
+
+size_t ffn_swiglu_nvfp4_lora_workspace_bytes(int M, int H, int I, int rank) {
+    if (M < 1 || M > 16 || H < 16 || I < 16 || rank < 1 || rank > nvf::kLoraMaxRank) return 0;
+    const LoraLayout l = lora_layout(M, H, I, rank, sms_for_sizing());
+    return l.ffn.fits ? l.total : 0;
+}
+
+nvfp4_status ffn_swiglu_nvfp4_lora(const void* x, int M, int H, int I, const void* gate_up_packed,
+                                   float gate_scale2, float up_scale2, const void* down_packed,
+                                   float down_scale2, nvfp4_act act, int rank, const void* gate_a,
+                                   const void* gate_b, const void* up_a, const void* up_b,
+                                   const void* down_a, const void* down_b, void* out, void* ws,
+                                   size_t ws_bytes, cudaStream_t stream) {
+    if (!ws) return NVFP4_ERR_NULL;
+    const int v = nvf::validate_ffn_args(x, M, H, I, gate_up_packed, down_packed, (int)act, out);
+    if (v != NVFP4_OK) return (nvfp4_status)v;
+    if (rank < 1 || rank > nvf::kLoraMaxRank) return NVFP4_ERR_RANGE;
+    const void* pa[3] = {gate_a, up_a, down_a};
+    const void* pb[3] = {gate_b, up_b, down_b};
+    for (int p = 0; p < 3; ++p) {
+        if ((pa[p] == nullptr) != (pb[p] == nullptr)) return NVFP4_ERR_NULL;
+        if (pa[p] && (!aligned16(pa[p]) || !aligned16(pb[p]))) return NVFP4_ERR_ALIGN;
+    }
+    if (!aligned16(ws)) return NVFP4_ERR_ALIGN;
+    const int sms = nvf::device_sm_count();
+    if (sms <= 0) return NVFP4_ERR_CUDA;
+    const LoraLayout l = lora_layout(M, H, I, rank, sms);
+    if (!l.ffn.fits) return NVFP4_ERR_SHAPE;
+    if (ws_bytes < l.total) return NVFP4_ERR_WORKSPACE;
+    char* w = reinterpret_cast<char*>(ws);
+    int* status = reinterpret_cast<int*>(w);
+    int* counters = reinterpret_cast<int*>(w + nvf::kStatusBytes);
+    void* h = w + l.ffn.h_off;
+    cudaError_t e = cudaSuccess;
+    // gate/up deltas of x, before the gate/up kernel
+    const void* A[2];
+    const void* B[2];
+    void* xa[2];
+    void* d[2];
+    int np = 0;
+    const void* deltas[2] = {nullptr, nullptr};
+    for (int p = 0; p < 2; ++p)
+        if (pa[p]) {
+            A[np] = pa[p];
+            B[np] = pb[p];
+            xa[np] = w + (p == 0 ? l.xa_g : l.xa_u);
+            d[np] = w + (p == 0 ? l.d_g : l.d_u);
+            deltas[p] = d[np];
+            ++np;
+        }
+    if (np > 0) {
+        e = nvf::launch_lora_xa(x, M, H, A, xa, np, rank, stream);
+        if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+        e = nvf::launch_lora_delta(xa, B, d, np, M, I, rank, false, stream);
+        if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    }
+    e = nvf::launch_stream_gemv(2, x, M, H, gate_up_packed, I, gate_scale2, up_scale2, (int)act, h,
+                                status, counters, w + l.ffn.dual_off, l.ffn.dual_bytes, sms, true,
+                                stream, np > 0 ? deltas : nullptr);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    void* xad = w + l.xa_d;
+    if (down_a) {  // A_down h, ahead of the down kernel
+        e = nvf::launch_lora_xa(h, M, I, &down_a, &xad, 1, rank, stream);
+        if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    }
+    e = nvf::launch_stream_gemv(1, h, M, I, down_packed, H, down_scale2, down_scale2, 0, out,
+                                status, counters + l.ffn.down_cnt_off / sizeof(int),
+                                w + l.ffn.down_off, l.ffn.down_bytes, sms, true, stream);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (down_a) {  // out = bf16(out + B_down xa_down)
+        const void* xac = xad;
+        e = nvf::launch_lora_delta(&xac, &down_b, &out, 1, M, H, rank, true, stream);
+        if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    }
+    return NVFP4_OK;
+}
+
+size_t nvfp4_lora_apply_scratch_bytes(int M, int rank) {
+    if (M < 1 || M > 16 || rank < 1 || rank > nvf::kLoraMaxRank) return 0;
+    return round256((size_t)M * rank * 2);
+}
+
+nvfp4_status nvfp4_lora_apply(const void* v, int M, int K, const void* a, const void* b, int rank,
+                              int N, void* base, void* scratch, size_t scratch_bytes,
+                              cudaStream_t stream) {
+    if (!v || !a || !b || !base || !scratch) return NVFP4_ERR_NULL;
+    if (M < 1 || M > 16 || rank < 1 || rank > nvf::kLoraMaxRank) return NVFP4_ERR_RANGE;
+    if (K < 2 || K % 2 != 0 || N < 1) return NVFP4_ERR_SHAPE;
+    if (!aligned16(v) || !aligned16(a) || !aligned16(b) || !aligned16(base) || !aligned16(scratch))
+        return NVFP4_ERR_ALIGN;
+    if (overlap(v, (size_t)M * K * 2, base, (size_t)M * N * 2)) return NVFP4_ERR_ALIAS;
+    if (scratch_bytes < nvfp4_lora_apply_scratch_bytes(M, rank)) return NVFP4_ERR_WORKSPACE;
+    cudaError_t e = nvf::launch_lora_xa(v, M, K, &a, &scratch, 1, rank, stream);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    const void* xa = scratch;
+    return cuda_status(nvf::launch_lora_delta(&xa, &b, &base, 1, M, N, rank, true, stream));
+}
+
 size_t ffn_gate_up_nvfp4_workspace_bytes(int M, int H, int I) {
     if (M < 1 || M > 16 || H < 16 || I < 16) return 0;
     return gemv_ws_bytes(2, M, I, H, sms_for_sizing());

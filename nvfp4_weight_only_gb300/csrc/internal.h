@@ -29,12 +29,26 @@ constexpr size_t kDataOffset = kStatusBytes + kCounterRegionBytes;
 // fp32 partial-sum bytes of one launch, and the counter bytes for N rows.
 size_t gemv_partial_bytes(int streams, int M, int N, int K, int num_sms);
 size_t gemv_counter_bytes(int N);
+// lora_deltas (streams == 2, may be null): bf16 [M, N] deltas added to the
+// rounded gate and up values before the activation, g = bf16(g + delta_g);
+// either entry may be null.
 cudaError_t launch_stream_gemv(int streams, const void* x, int M, int K, const void* packed, int N,
                                float scale_a, float scale_b, int act, void* out, int* status,
                                int* counters, void* partials, size_t partial_bytes, int num_sms,
-                               bool early_weights, cudaStream_t s);
+                               bool early_weights, cudaStream_t s,
+                               const void* const* lora_deltas = nullptr);
 
 int device_sm_count();
+
+// lora.cu: the adapter overlay, dW = B A (A [r, K], B [N, r], bf16).
+constexpr int kLoraMaxRank = 64;
+// xa[p] [M, r] = bf16(A[p] v) for each of `pairs` (1 or 2) matrices A[p] [r, K].
+cudaError_t launch_lora_xa(const void* v, int M, int K, const void* const* A, void* const* xa,
+                           int pairs, int r, cudaStream_t s);
+// d = bf16(B[p] xa[p]) [M, N]: stored in out[p] (add false) or added to it as
+// out[p] = bf16(out[p] + d) (add true).
+cudaError_t launch_lora_delta(const void* const* xa, const void* const* B, void* const* out,
+                              int pairs, int M, int N, int r, bool add, cudaStream_t s);
 
 // Whether the kernel's shared-memory plan for this problem has the alignment
 // its accesses assume (the launcher refuses plans that do not).

@@ -205,6 +205,9 @@ struct KArgs {
     // L * R < 2^32: the range arithmetic below runs on FastDiv multiplies
     int fast;
     FastDiv div_R, div_L, div_CS;
+    // adapter deltas for gate and up (bf16 [M, N], null when absent)
+    const __nv_bfloat16* lora_dg;
+    const __nv_bfloat16* lora_du;
 };
 
 __device__ __forceinline__ long long range_start(const KArgs& a, long long r) {
@@ -290,8 +293,16 @@ __device__ __forceinline__ void store_output(const KArgs& a, int row, int token,
     if (NS == 1) {
         a.out[(size_t)token * a.N + row] = __float2bfloat16_rn(va * a.scale_a);
     } else {
-        const float gb = __bfloat162float(__float2bfloat16_rn(va * a.scale_a));
-        const float ub = __bfloat162float(__float2bfloat16_rn(vb * a.scale_b));
+        float gb = __bfloat162float(__float2bfloat16_rn(va * a.scale_a));
+        float ub = __bfloat162float(__float2bfloat16_rn(vb * a.scale_b));
+        // adapter deltas land on the rounded projections, before the
+        // activation; a bf16 plus a bf16 rounds once, exactly, through fp32
+        if (a.lora_dg != nullptr)
+            gb = __bfloat162float(__float2bfloat16_rn(
+                gb + __bfloat162float(a.lora_dg[(size_t)token * a.N + row])));
+        if (a.lora_du != nullptr)
+            ub = __bfloat162float(__float2bfloat16_rn(
+                ub + __bfloat162float(a.lora_du[(size_t)token * a.N + row])));
         a.out[(size_t)token * a.N + row] = gated_product(a.act, gb, ub);
     }
 }
@@ -1276,7 +1287,8 @@ static cudaError_t launch_t(const Plan& p, const KArgs& a, cudaStream_t s) {
 cudaError_t launch_stream_gemv(int streams, const void* x, int M, int K, const void* packed, int N,
                                float scale_a, float scale_b, int act, void* out, int* status,
                                int* counters, void* partials, size_t partial_bytes, int num_sms,
-                               bool early_weights, cudaStream_t s) {
+                               bool early_weights, cudaStream_t s,
+                               const void* const* lora_deltas) {
     const Plan p = make_plan(streams, M, N, K, num_sms);
     if (partial_bytes < p.total || !plan_aligned(p)) return cudaErrorInvalidValue;
     KArgs a;
@@ -1310,6 +1322,9 @@ cudaError_t launch_stream_gemv(int streams, const void* x, int M, int K, const v
     a.early_weights = early_weights ? 1 : 0;
     a.wait_ns = g_test_wait_ns.load();
     a.stall = g_test_stall.load();
+    a.lora_dg = lora_deltas ? reinterpret_cast<const __nv_bfloat16*>(lora_deltas[0]) : nullptr;
+    a.lora_du = lora_deltas ? reinterpret_cast<const __nv_bfloat16*>(lora_deltas[1]) : nullptr;
+    if (streams != 2 && lora_deltas != nullptr) return cudaErrorInvalidValue;
     a.fast = (unsigned long long)p.L * (unsigned long long)p.R < (1ull << 32) ? 1 : 0;
     a.div_R = FastDiv::make((unsigned)p.R);
     a.div_L = FastDiv::make((unsigned)(p.L < (1LL << 32) ? p.L : 1));

@@ -33,6 +33,8 @@ EXPORTS = [
     "ffn_swiglu_nvfp4_hidden_offset",
     "ffn_swiglu_nvfp4", "ffn_gate_up_nvfp4_workspace_bytes", "ffn_gate_up_nvfp4",
     "ffn_swiglu_nvfp4_noalloc", "nvfp4_noalloc_status",
+    "ffn_swiglu_nvfp4_lora_workspace_bytes", "ffn_swiglu_nvfp4_lora",
+    "nvfp4_lora_apply_scratch_bytes", "nvfp4_lora_apply",
     "nvfp4_workspace_init", "nvfp4_workspace_status", "nvfp4_status_string",
 ]
 # Every symbol declared in include/nvfp4ffn_testing.h (test hooks).
@@ -79,6 +81,11 @@ def load(build_if_missing: bool = False):
         "ffn_gate_up_nvfp4": (i32, [vp, i32, i32, i32, vp, f32, f32, i32, vp, vp, sz, vp]),
         "ffn_swiglu_nvfp4_noalloc": (i32, [vp, i32, i32, i32, vp, f32, f32, vp, f32, i32, vp, vp]),
         "nvfp4_noalloc_status": (i32, [vp]),
+        "ffn_swiglu_nvfp4_lora_workspace_bytes": (sz, [i32, i32, i32, i32]),
+        "ffn_swiglu_nvfp4_lora": (i32, [vp, i32, i32, i32, vp, f32, f32, vp, f32, i32, i32,
+                                        vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "nvfp4_lora_apply_scratch_bytes": (sz, [i32, i32]),
+        "nvfp4_lora_apply": (i32, [vp, i32, i32, vp, vp, i32, i32, vp, vp, sz, vp]),
         "nvfp4_testing_inject_stall": (i32, [i32, ctypes.c_ulonglong]),
         "nvfp4_testing_plan_aligned": (i32, [i32, i32, i32, i32, i32]),
         "nvfp4_workspace_init": (i32, [vp, sz, vp]),
@@ -243,6 +250,52 @@ def ffn_swiglu_nvfp4_noalloc(x: torch.Tensor, gate_up_packed: torch.Tensor, gate
                                       float(up_scale2), _ptr(down_packed), float(down_scale2),
                                       int(act), _ptr(out), _stream(x.device)))
     return out
+
+
+def ffn_swiglu_nvfp4_lora(x: torch.Tensor, gate_up_packed: torch.Tensor, gate_scale2: float,
+                          up_scale2: float, down_packed: torch.Tensor, down_scale2: float, I: int,
+                          act: int = NVFP4_ACT_SILU, gate=None, up=None, down=None,
+                          ws: torch.Tensor = None, out: torch.Tensor = None) -> torch.Tensor:
+    """The FFN with the LoRA overlay; gate/up/down = (A, B) bf16 pairs or None."""
+    _cuda(x, "x", torch.bfloat16)
+    M, H = x.shape
+    pairs = [gate, up, down]
+    rank = next((p[0].shape[0] for p in pairs if p is not None), 1)
+    for p in pairs:
+        if p is not None:
+            _cuda(p[0], "lora A", torch.bfloat16)
+            _cuda(p[1], "lora B", torch.bfloat16)
+    L = load()
+    if ws is None:
+        ws = workspace(L.ffn_swiglu_nvfp4_lora_workspace_bytes(M, H, I, rank), x.device)
+    if out is None:
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    _cuda(out, "out", torch.bfloat16)
+    ptrs = []
+    for p in pairs:
+        ptrs += [_ptr(p[0]), _ptr(p[1])] if p is not None else [_ptr(None), _ptr(None)]
+    _check("ffn_swiglu_nvfp4_lora",
+           L.ffn_swiglu_nvfp4_lora(_ptr(x), M, H, I, _ptr(gate_up_packed), float(gate_scale2),
+                                   float(up_scale2), _ptr(down_packed), float(down_scale2),
+                                   int(act), rank, *ptrs, _ptr(out), _ptr(ws), ws.numel(),
+                                   _stream(x.device)))
+    return out
+
+
+def nvfp4_lora_apply(v: torch.Tensor, a: torch.Tensor, b: torch.Tensor,
+                     base: torch.Tensor) -> torch.Tensor:
+    """base [M, N] = bf16(base + bf16(b bf16(a v))) in place (returns base)."""
+    for n, t in (("v", v), ("a", a), ("b", b), ("base", base)):
+        _cuda(t, n, torch.bfloat16)
+    M, K = v.shape
+    rank = a.shape[0]
+    N = b.shape[0]
+    L = load()
+    scratch = workspace(L.nvfp4_lora_apply_scratch_bytes(M, rank), v.device)
+    _check("nvfp4_lora_apply",
+           L.nvfp4_lora_apply(_ptr(v), M, K, _ptr(a), _ptr(b), rank, N, _ptr(base),
+                              _ptr(scratch), scratch.numel(), _stream(v.device)))
+    return base
 
 
 def ffn_gate_up_nvfp4_workspace_bytes(M: int, H: int, I: int) -> int:

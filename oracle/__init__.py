@@ -62,6 +62,19 @@ def lib():
         L.orc_bf16_from_double_array.restype = None
         L.orc_act_array.argtypes = [f64p, i64, ctypes.c_int, f64p]
         L.orc_act_array.restype = None
+        L.orc_lora_xa.argtypes = [u16p, i64, i64, u16p, i64, u16p]
+        L.orc_lora_xa.restype = None
+        L.orc_lora_delta.argtypes = [u16p, i64, i64, u16p, i64, u16p]
+        L.orc_lora_delta.restype = None
+        L.orc_lora_add.argtypes = [u16p, u16p, i64]
+        L.orc_lora_add.restype = None
+        L.orc_lora_apply.argtypes = [u16p, i64, i64, u16p, u16p, i64, i64, u16p]
+        L.orc_lora_apply.restype = None
+        vp = ctypes.c_void_p
+        L.orc_ffn_lora.argtypes = [u16p, i64, i64, i64, u8p, u8p, ctypes.c_float,
+                                   u8p, u8p, ctypes.c_float, u8p, u8p, ctypes.c_float,
+                                   ctypes.c_int, i64, vp, vp, vp, vp, vp, vp, u16p, u16p]
+        L.orc_ffn_lora.restype = None
         L.orc_set_threads.argtypes = [ctypes.c_int]
         L.orc_set_threads.restype = ctypes.c_int
         _lib = L
@@ -208,3 +221,72 @@ def bf16_bits_to_f64(bits):
     """Exact widening of bf16 bit patterns to float64 (numpy bit shift)."""
     b = np.asarray(bits, np.uint16).astype(np.uint32) << 16
     return b.view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------- LoRA overlay
+
+def lora_xa(v_bits, A_bits):
+    """xa bf16 bits [M, r] = bf16(A v) for v bf16 [M, K], A bf16 [r, K]."""
+    v = _c(v_bits, np.uint16)
+    A = _c(A_bits, np.uint16)
+    M, K = v.shape
+    r = A.shape[0]
+    xa = np.zeros((M, r), np.uint16)
+    lib().orc_lora_xa(v, M, K, A, r, xa)
+    return xa
+
+
+def lora_delta(xa_bits, B_bits):
+    """delta bf16 bits [M, N] = bf16(B xa) for xa [M, r], B bf16 [N, r]."""
+    xa = _c(xa_bits, np.uint16)
+    B = _c(B_bits, np.uint16)
+    M, r = xa.shape
+    N = B.shape[0]
+    d = np.zeros((M, N), np.uint16)
+    lib().orc_lora_delta(xa, M, r, B, N, d)
+    return d
+
+
+def lora_add(base_bits, delta_bits):
+    """bf16(base + delta), elementwise (returns a new array)."""
+    out = np.array(base_bits, np.uint16, copy=True, order="C")
+    lib().orc_lora_add(out.reshape(-1), _c(delta_bits, np.uint16).reshape(-1), out.size)
+    return out
+
+
+def lora_apply(v_bits, A_bits, B_bits, base_bits):
+    """base + dW v with dW = B A (returns a new array)."""
+    v = _c(v_bits, np.uint16)
+    M, K = v.shape
+    A = _c(A_bits, np.uint16)
+    B = _c(B_bits, np.uint16)
+    out = np.array(base_bits, np.uint16, copy=True, order="C")
+    lib().orc_lora_apply(v, M, K, A, B, A.shape[0], B.shape[0], out)
+    return out
+
+
+def ffn_lora(x_bits, I, gate, up, down, act=ACT_SILU, lora=None):
+    """FFN with the LoRA overlay.  lora = dict(rank=r, gate=(A, B) or None,
+    up=..., down=...) with bf16-bit arrays.  Returns (out [M, H], h [M, I])."""
+    x = _c(x_bits, np.uint16)
+    M, H = x.shape
+    lora = lora or {}
+    r = int(lora.get("rank", 1))
+    keep = []
+
+    def ptr(pair, i):
+        if not pair:
+            return None
+        a = _c(pair[i], np.uint16)
+        keep.append(a)
+        return a.ctypes.data
+
+    out = np.zeros((M, H), np.uint16)
+    h = np.zeros((M, I), np.uint16)
+    lib().orc_ffn_lora(x, M, H, I, _c(gate[0], np.uint8), _c(gate[1], np.uint8), gate[2],
+                       _c(up[0], np.uint8), _c(up[1], np.uint8), up[2],
+                       _c(down[0], np.uint8), _c(down[1], np.uint8), down[2], int(act), r,
+                       ptr(lora.get("gate"), 0), ptr(lora.get("gate"), 1),
+                       ptr(lora.get("up"), 0), ptr(lora.get("up"), 1),
+                       ptr(lora.get("down"), 0), ptr(lora.get("down"), 1), out, h)
+    return out, h

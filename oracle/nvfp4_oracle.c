@@ -354,6 +354,108 @@ void orc_ffn(const uint16_t *x, int64_t M, int64_t H, int64_t I,
     free(h);
 }
 
+/* ---------------- LoRA overlay ---------------- */
+
+/*
+ * The dense-FFN page's adapter overlay (DenseFfnLayer::apply_lora_gate_up and
+ * apply_lora_down): gate_out += dW_gate x and up_out += dW_up x land after the
+ * gate/up projections and before the activation; output += dW_down act lands
+ * after the down projection and contracts over the activation h, not over the
+ * layer input.  Readings (the page names the helper's buffers, lora_xa and
+ * lora_delta, but not their types or formulas):
+ *   dW = B A with A [r, in] and B [out, r], both bf16, any alpha/r folded into B;
+ *   xa = bf16(A v), delta = bf16(B xa) (every named buffer holds bf16, like the
+ *   engine's other activations), base = bf16(base + delta).
+ */
+
+/* xa bf16 [M, r] = bf16(sum_k A[j][k] v[m][k]) for v bf16 [M, K], A bf16 [r, K]. */
+void orc_lora_xa(const uint16_t *v, int64_t M, int64_t K, const uint16_t *A, int64_t r,
+                 uint16_t *xa)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t j = 0; j < r; ++j) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += orc_bf16_decode(A[j * K + k]) * orc_bf16_decode(v[m * K + k]);
+            xa[m * r + j] = orc_bf16_from_double(acc);
+        }
+}
+
+/* delta bf16 [M, N] = bf16(sum_j B[n][j] xa[m][j]) for xa bf16 [M, r], B bf16 [N, r]. */
+void orc_lora_delta(const uint16_t *xa, int64_t M, int64_t r, const uint16_t *B, int64_t N,
+                    uint16_t *delta)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < r; ++j)
+                acc += orc_bf16_decode(B[n * r + j]) * orc_bf16_decode(xa[m * r + j]);
+            delta[m * N + n] = orc_bf16_from_double(acc);
+        }
+}
+
+/* base[i] = bf16(base[i] + delta[i]) for i < n (both bf16). */
+void orc_lora_add(uint16_t *base, const uint16_t *delta, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        base[i] = orc_bf16_from_double(orc_bf16_decode(base[i]) + orc_bf16_decode(delta[i]));
+}
+
+/* base bf16 [M, N] += dW v for v bf16 [M, K] (the page's apply_lora_delta). */
+void orc_lora_apply(const uint16_t *v, int64_t M, int64_t K, const uint16_t *A,
+                    const uint16_t *B, int64_t r, int64_t N, uint16_t *base)
+{
+    uint16_t *xa = (uint16_t *)malloc((size_t)(M * r > 0 ? M * r : 1) * 2);
+    uint16_t *d = (uint16_t *)malloc((size_t)(M * N > 0 ? M * N : 1) * 2);
+    if (xa && d) {
+        orc_lora_xa(v, M, K, A, r, xa);
+        orc_lora_delta(xa, M, r, B, N, d);
+        orc_lora_add(base, d, M * N);
+    }
+    free(xa);
+    free(d);
+}
+
+/*
+ * The FFN with the overlay (a pair whose A is NULL is absent):
+ *   g = bf16(gemv_gate x) [+ dW_gate x],  u = bf16(gemv_up x) [+ dW_up x],
+ *   h = bf16(act(g) u),  out = bf16(gemv_down h) [+ dW_down h].
+ * h (bf16 [M, I]) is also returned when h_out is not NULL.
+ */
+void orc_ffn_lora(const uint16_t *x, int64_t M, int64_t H, int64_t I,
+                  const uint8_t *gc, const uint8_t *gs, float g2,
+                  const uint8_t *uc, const uint8_t *us, float u2,
+                  const uint8_t *dc, const uint8_t *ds, float d2, int act, int64_t r,
+                  const uint16_t *gA, const uint16_t *gB, const uint16_t *uA,
+                  const uint16_t *uB, const uint16_t *dA, const uint16_t *dB,
+                  uint16_t *out, uint16_t *h_out)
+{
+    size_t n = (size_t)(M * I > 0 ? M * I : 1);
+    uint16_t *g = (uint16_t *)malloc(n * 2), *u = (uint16_t *)malloc(n * 2);
+    uint16_t *h = (uint16_t *)malloc(n * 2);
+    if (g && u && h) {
+        orc_gemv(x, M, H, gc, gs, g2, I, g);
+        orc_gemv(x, M, H, uc, us, u2, I, u);
+        if (gA)
+            orc_lora_apply(x, M, H, gA, gB, r, I, g);
+        if (uA)
+            orc_lora_apply(x, M, H, uA, uB, r, I, u);
+        for (int64_t i = 0; i < M * I; ++i) {
+            double gv = orc_bf16_decode(g[i]), uv = orc_bf16_decode(u[i]);
+            double a = (act == 0) ? orc_silu(gv) : orc_gelu_tanh(gv);
+            h[i] = orc_bf16_from_double(a * uv);
+        }
+        orc_gemv(h, M, I, dc, ds, d2, H, out);
+        if (dA)
+            orc_lora_apply(h, M, I, dA, dB, r, H, out);
+        if (h_out)
+            memcpy(h_out, h, (size_t)(M * I) * 2);
+    }
+    free(g);
+    free(u);
+    free(h);
+}
+
 int orc_set_threads(int n)
 {
 #ifdef _OPENMP

@@ -72,13 +72,19 @@ def check_gemv(y_bits, x_bits, q, N, what="gemv", acc_eps=ACC_EPS):
 
 
 def hidden_interval(x_bits, gate, up, act, acc_eps=ACC_EPS):
-    """Interval of valid h = bf16(act(g) * u) [M, I]: g and u range over the
-    roundings their interval allows, act over its range on the g interval
-    (monotone pieces plus the interior minimum), the product over the box
-    corners, widened by the kernel's fp32 activation error."""
+    """Interval of valid h = bf16(act(g) * u) [M, I] for g and u the rounded
+    gate and up projections of x (gemv_interval each)."""
     I = gate[0].shape[0]
     g_lo, g_hi = gemv_interval(x_bits, gate, I, acc_eps)
     u_lo, u_hi = gemv_interval(x_bits, up, I, acc_eps)
+    return hidden_interval_from(g_lo, g_hi, u_lo, u_hi, act)
+
+
+def hidden_interval_from(g_lo, g_hi, u_lo, u_hi, act):
+    """Interval of valid h = bf16(act(g) * u) for g in [g_lo, g_hi] and u in
+    [u_lo, u_hi] (bf16 values): act over its range on the g interval (monotone
+    pieces plus the interior minimum), the product over the box corners,
+    widened by the kernel's fp32 activation error."""
     a1, a2 = oracle.act_array(g_lo, act), oracle.act_array(g_hi, act)
     a_lo, a_hi = np.minimum(a1, a2), np.maximum(a1, a2)
     t_min = ACT_MIN_T[act]
@@ -119,3 +125,33 @@ def round_toward_zero_bf16(v):
     away = np.abs(r) > np.abs(v)
     mag = np.where(away & ((bits & 0x7FFF) > 0), (bits & 0x7FFF) - 1, bits & 0x7FFF)
     return ((bits & 0x8000) | mag).astype(np.uint16)
+
+
+def bf16_f64(bits):
+    return oracle.bf16_bits_to_f64(np.asarray(bits, np.uint16))
+
+
+def lora_delta_interval(v_lo, v_hi, A_bits, B_bits, acc_eps=ACC_EPS):
+    """Interval of the adapter delta d = bf16(B bf16(A v)) [M, N] for v in the
+    box [v_lo, v_hi] (float64 arrays [M, K] of bf16 values): A v over the box
+    (interval arithmetic), its bf16 rounding interval with the fp32
+    accumulation window, then B xa over the xa box likewise."""
+    A = bf16_f64(A_bits)
+    B = bf16_f64(B_bits)
+
+    def box_matmul(lo, hi, W):  # [lo, hi] @ W.T elementwise-exact bounds
+        Wp, Wn = np.maximum(W, 0.0), np.minimum(W, 0.0)
+        return lo @ Wp.T + hi @ Wn.T, hi @ Wp.T + lo @ Wn.T
+
+    mag = np.maximum(np.abs(v_lo), np.abs(v_hi))
+    s_lo, s_hi = box_matmul(v_lo, v_hi, A)
+    w = acc_eps * (mag @ np.abs(A).T)
+    xa_lo, xa_hi = bf16_round(s_lo - w), bf16_round(s_hi + w)
+    d_lo, d_hi = box_matmul(xa_lo, xa_hi, B)
+    wd = acc_eps * (np.maximum(np.abs(xa_lo), np.abs(xa_hi)) @ np.abs(B).T)
+    return bf16_round(d_lo - wd), bf16_round(d_hi + wd)
+
+
+def check_interval(got_bits, lo, hi, ref_bits, what):
+    """got inside [lo, hi] everywhere, equal to ref wherever lo == hi."""
+    return _stats(bf16_f64(got_bits), lo, hi, bf16_f64(ref_bits), what)
