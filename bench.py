@@ -463,6 +463,9 @@ def run_sweep(args, ffi, synth, dev, timer, sampler, layers, H, I, peak):
     for M in range(1, 17):
         head[f"M{M}"] = ffn_case(layers, H, I, M, 0, 0.0, kernels=True)
     res[f"ffn_{H}x{I}_silu"] = head
+    # verify batches / small prefill beyond one kernel group (16 rows)
+    res[f"ffn_{H}x{I}_silu_large_batches"] = {f"M{M}": ffn_case(layers, H, I, M, 0, 0.0)
+                                              for M in (17, 24, 32, 48, 64)}
     bm = {}
     for M in (4, 8, 16):
         for act, name in ((0, "silu"), (1, "gelu_tanh")):

@@ -56,7 +56,7 @@ typedef enum {
     NVFP4_ERR_NULL = 1,      /* a required pointer is NULL */
     NVFP4_ERR_SHAPE = 2,     /* a size is <= 0, or K/H/I is not a multiple of 16 */
     NVFP4_ERR_ALIGN = 3,     /* a device pointer is not 16-byte aligned */
-    NVFP4_ERR_RANGE = 4,     /* M outside [1, 16], or an unknown enum value */
+    NVFP4_ERR_RANGE = 4,     /* M outside the call's range, or an unknown enum value */
     NVFP4_ERR_WORKSPACE = 5, /* workspace smaller than the size query returns */
     NVFP4_ERR_CUDA = 6,      /* a CUDA runtime call or launch failed */
     NVFP4_ERR_TIMEOUT = 7,   /* a kernel gave up on a bounded wait (device status word) */
@@ -145,9 +145,12 @@ size_t nvfp4_gemv_workspace_bytes(int M, int N, int K);
  *   y[m, n] = bf16( scale2 * sum_k x[m, k] * E2M1(c[n, k]) * E4M3(s[n, k/16]) )
  *   x (device) bf16 [M, K];  packed_w (device) from nvfp4_repack(N, K);
  *   y (device, out) bf16 [M, N];  ws (device) >= nvfp4_gemv_workspace_bytes.
- * Requirements: 1 <= M <= 16, N >= 1, K >= 16, K % 16 == 0, x and y disjoint.
+ * Requirements: 1 <= M <= 64, N >= 1, K >= 16, K % 16 == 0, x and y disjoint.
  * Accumulation is fp32 on exactly dequantised weights; every x row is scaled
  * by a power of two into the fp16 operand range, so any finite bf16 x works.
+ * The kernels take up to 16 token rows at a time: M > 16 (a verify batch or a
+ * small prefill, the page's forward_prefill range M <= 64) runs as groups of
+ * 16 rows and a remainder, each group streaming the weights once.
  */
 nvfp4_status nvfp4_gemv(const void* x, int M, int K, const void* packed_w, float scale2,
                         int N, void* y, void* ws, size_t ws_bytes, cudaStream_t stream);
@@ -172,8 +175,9 @@ size_t ffn_swiglu_nvfp4_hidden_offset(void);
  *   x (device) bf16 [M, H];  gate_up_packed (device) from
  *   nvfp4_repack_gate_up(I, H);  down_packed (device) from nvfp4_repack(H, I);
  *   out (device, out) bf16 [M, H];  ws (device) >= ffn_swiglu_nvfp4_workspace_bytes.
- * Requirements: 1 <= M <= 16, H and I >= 16 and multiples of 16, x and out
- * disjoint, act a nvfp4_act value.
+ * Requirements: 1 <= M <= 64, H and I >= 16 and multiples of 16, x and out
+ * disjoint, act a nvfp4_act value.  M > 16 runs in groups of 16 rows, as for
+ * nvfp4_gemv.
  */
 nvfp4_status ffn_swiglu_nvfp4(const void* x, int M, int H, int I,
                               const void* gate_up_packed, float gate_scale2, float up_scale2,
@@ -219,7 +223,8 @@ size_t ffn_swiglu_nvfp4_lora_workspace_bytes(int M, int H, int I, int rank);
  * down_b [H, r] (device, bf16); a pair given as two NULL pointers is absent
  * (its delta is zero).  A pair with one NULL pointer is NVFP4_ERR_NULL; rank
  * outside [1, 64] is NVFP4_ERR_RANGE.  Other arguments and requirements as
- * ffn_swiglu_nvfp4.  Up to four small launches join the FFN's two.
+ * ffn_swiglu_nvfp4, except 1 <= M <= 16.  Up to four small launches join the
+ * FFN's two.
  */
 nvfp4_status ffn_swiglu_nvfp4_lora(const void* x, int M, int H, int I,
                                    const void* gate_up_packed, float gate_scale2,
@@ -244,8 +249,8 @@ nvfp4_status nvfp4_lora_apply(const void* v, int M, int K, const void* a, const 
                               cudaStream_t stream);
 
 /*
- * ffn_swiglu_nvfp4 for callers that cannot allocate device memory where they
- * run the FFN (a process that reserves the device's memory for its own pool at
+ * ffn_swiglu_nvfp4 (1 <= M <= 16) for callers that cannot allocate device
+ * memory where they run the FFN (a process that reserves the device's memory for its own pool at
  * start-up and forbids later cudaMalloc, or code that must not risk the
  * implicit device synchronisation of an allocation).  The pages have no
  * counterpart of this call; it exists for such callers.

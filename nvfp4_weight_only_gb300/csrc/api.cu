@@ -31,11 +31,32 @@ nvfp4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : N
 
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
+// Token rows per call: up to kMaxTokens; the kernels take groups of up to
+// kGroupTokens rows, so a larger batch runs as consecutive groups, each of
+// which streams the weights once.
+constexpr int kMaxTokens = 64;
+constexpr int kGroupTokens = 16;
+
+int group_count(int M) { return (M + kGroupTokens - 1) / kGroupTokens; }
+int group_rows(int M, int g) {
+    const int left = M - g * kGroupTokens;
+    return left < kGroupTokens ? left : kGroupTokens;
+}
+
+// Partial-sum bytes of the largest launch among M's groups (they run one
+// after another on the same stream, so they share one area).
+size_t group_partial_bytes(int streams, int M, int N, int K, int sms) {
+    size_t most = nvf::gemv_partial_bytes(streams, group_rows(M, 0), N, K, sms);
+    const int last = group_rows(M, group_count(M) - 1);
+    const size_t b = nvf::gemv_partial_bytes(streams, last, N, K, sms);
+    return b > most ? b : most;
+}
+
 // GEMV workspace: [status][counter region][partials].  0 if N has more row
 // blocks than the counter region holds.
 size_t gemv_ws_bytes(int streams, int M, int N, int K, int sms) {
     if (nvf::gemv_counter_bytes(N) > nvf::kCounterRegionBytes) return 0;
-    return nvf::kDataOffset + round256(nvf::gemv_partial_bytes(streams, M, N, K, sms));
+    return nvf::kDataOffset + round256(group_partial_bytes(streams, M, N, K, sms));
 }
 
 // FFN workspace: [status][counter region: dual's counters, then down's]
@@ -51,9 +72,9 @@ FfnLayout ffn_layout(int M, int H, int I, int sms) {
     l.fits = l.down_cnt_off + nvf::gemv_counter_bytes(H) <= nvf::kCounterRegionBytes;
     l.h_off = nvf::kDataOffset;
     l.dual_off = l.h_off + round256((size_t)M * I * 2);
-    l.dual_bytes = round256(nvf::gemv_partial_bytes(2, M, I, H, sms));
+    l.dual_bytes = round256(group_partial_bytes(2, M, I, H, sms));
     l.down_off = l.dual_off + l.dual_bytes;
-    l.down_bytes = round256(nvf::gemv_partial_bytes(1, M, H, I, sms));
+    l.down_bytes = round256(group_partial_bytes(1, M, H, I, sms));
     l.total = l.down_off + l.down_bytes;
     return l;
 }
@@ -65,7 +86,7 @@ namespace nvf {
 int validate_ffn_args(const void* x, int M, int H, int I, const void* gate_up_packed,
                       const void* down_packed, int act, const void* out) {
     if (!x || !gate_up_packed || !down_packed || !out) return NVFP4_ERR_NULL;
-    if (M < 1 || M > 16) return NVFP4_ERR_RANGE;
+    if (M < 1 || M > kMaxTokens) return NVFP4_ERR_RANGE;
     if (act != NVFP4_ACT_SILU && act != NVFP4_ACT_GELU_TANH) return NVFP4_ERR_RANGE;
     if (H < 16 || I < 16 || H % 16 != 0 || I % 16 != 0) return NVFP4_ERR_SHAPE;
     if (!aligned16(x) || !aligned16(gate_up_packed) || !aligned16(down_packed) ||
@@ -147,14 +168,14 @@ nvfp4_status nvfp4_unpack(const void* packed, int N, int K, uint8_t* codes, uint
 }
 
 size_t nvfp4_gemv_workspace_bytes(int M, int N, int K) {
-    if (M < 1 || M > 16 || N < 1 || K < 16) return 0;
+    if (M < 1 || M > kMaxTokens || N < 1 || K < 16) return 0;
     return gemv_ws_bytes(1, M, N, K, sms_for_sizing());
 }
 
 nvfp4_status nvfp4_gemv(const void* x, int M, int K, const void* packed_w, float scale2, int N,
                         void* y, void* ws, size_t ws_bytes, cudaStream_t stream) {
     if (!x || !packed_w || !y || !ws) return NVFP4_ERR_NULL;
-    if (M < 1 || M > 16) return NVFP4_ERR_RANGE;
+    if (M < 1 || M > kMaxTokens) return NVFP4_ERR_RANGE;
     if (N < 1 || K < 16 || K % 16 != 0) return NVFP4_ERR_SHAPE;
     if (!aligned16(x) || !aligned16(packed_w) || !aligned16(y) || !aligned16(ws))
         return NVFP4_ERR_ALIGN;
@@ -165,14 +186,20 @@ nvfp4_status nvfp4_gemv(const void* x, int M, int K, const void* packed_w, float
     if (need == 0) return NVFP4_ERR_SHAPE;
     if (ws_bytes < need) return NVFP4_ERR_WORKSPACE;
     char* w = reinterpret_cast<char*>(ws);
-    return cuda_status(nvf::launch_stream_gemv(
-        1, x, M, K, packed_w, N, scale2, scale2, 0, y, reinterpret_cast<int*>(w),
-        reinterpret_cast<int*>(w + nvf::kStatusBytes), w + nvf::kDataOffset,
-        need - nvf::kDataOffset, sms, true, stream));
+    for (int g = 0; g < group_count(M); ++g) {
+        const size_t r0 = (size_t)g * kGroupTokens;
+        const cudaError_t e = nvf::launch_stream_gemv(
+            1, reinterpret_cast<const char*>(x) + r0 * K * 2, group_rows(M, g), K, packed_w, N,
+            scale2, scale2, 0, reinterpret_cast<char*>(y) + r0 * N * 2, reinterpret_cast<int*>(w),
+            reinterpret_cast<int*>(w + nvf::kStatusBytes), w + nvf::kDataOffset,
+            need - nvf::kDataOffset, sms, true, stream);
+        if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    }
+    return NVFP4_OK;
 }
 
 size_t ffn_swiglu_nvfp4_workspace_bytes(int M, int H, int I) {
-    if (M < 1 || M > 16 || H < 16 || I < 16) return 0;
+    if (M < 1 || M > kMaxTokens || H < 16 || I < 16) return 0;
     const FfnLayout l = ffn_layout(M, H, I, sms_for_sizing());
     return l.fits ? l.total : 0;
 }
@@ -196,14 +223,22 @@ nvfp4_status ffn_swiglu_nvfp4(const void* x, int M, int H, int I, const void* ga
     int* status = reinterpret_cast<int*>(w);
     int* counters = reinterpret_cast<int*>(w + nvf::kStatusBytes);
     void* h = w + l.h_off;
-    cudaError_t e = nvf::launch_stream_gemv(2, x, M, H, gate_up_packed, I, gate_scale2, up_scale2,
-                                            (int)act, h, status, counters, w + l.dual_off,
-                                            l.dual_bytes, sms, true, stream);
-    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
-    e = nvf::launch_stream_gemv(1, h, M, I, down_packed, H, down_scale2, down_scale2, 0, out,
-                                status, counters + l.down_cnt_off / sizeof(int), w + l.down_off,
-                                l.down_bytes, sms, true, stream);
-    return cuda_status(e);
+    for (int g = 0; g < group_count(M); ++g) {
+        const size_t r0 = (size_t)g * kGroupTokens;
+        const int mg = group_rows(M, g);
+        char* hg = reinterpret_cast<char*>(h) + r0 * I * 2;
+        cudaError_t e = nvf::launch_stream_gemv(
+            2, reinterpret_cast<const char*>(x) + r0 * H * 2, mg, H, gate_up_packed, I,
+            gate_scale2, up_scale2, (int)act, hg, status, counters, w + l.dual_off, l.dual_bytes,
+            sms, true, stream);
+        if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+        e = nvf::launch_stream_gemv(1, hg, mg, I, down_packed, H, down_scale2, down_scale2, 0,
+                                    reinterpret_cast<char*>(out) + r0 * H * 2, status,
+                                    counters + l.down_cnt_off / sizeof(int), w + l.down_off,
+                                    l.down_bytes, sms, true, stream);
+        if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    }
+    return NVFP4_OK;
 }
 
 // LoRA FFN workspace: the FFN's, then xa_gate [M, r], xa_up [M, r], the gate
@@ -241,7 +276,7 @@ nvfp4_status ffn_swiglu_nvfp4_lora(const void* x, int M, int H, int I, const voi
     if (!ws) return NVFP4_ERR_NULL;
     const int v = nvf::validate_ffn_args(x, M, H, I, gate_up_packed, down_packed, (int)act, out);
     if (v != NVFP4_OK) return (nvfp4_status)v;
-    if (rank < 1 || rank > nvf::kLoraMaxRank) return NVFP4_ERR_RANGE;
+    if (M > kGroupTokens || rank < 1 || rank > nvf::kLoraMaxRank) return NVFP4_ERR_RANGE;
     const void* pa[3] = {gate_a, up_a, down_a};
     const void* pb[3] = {gate_b, up_b, down_b};
     for (int p = 0; p < 3; ++p) {
@@ -324,7 +359,7 @@ nvfp4_status nvfp4_lora_apply(const void* v, int M, int K, const void* a, const 
 }
 
 size_t ffn_gate_up_nvfp4_workspace_bytes(int M, int H, int I) {
-    if (M < 1 || M > 16 || H < 16 || I < 16) return 0;
+    if (M < 1 || M > kMaxTokens || H < 16 || I < 16) return 0;
     return gemv_ws_bytes(2, M, I, H, sms_for_sizing());
 }
 
@@ -332,7 +367,7 @@ nvfp4_status ffn_gate_up_nvfp4(const void* x, int M, int H, int I, const void* g
                                float gate_scale2, float up_scale2, nvfp4_act act, void* h,
                                void* ws, size_t ws_bytes, cudaStream_t stream) {
     if (!x || !gate_up_packed || !h || !ws) return NVFP4_ERR_NULL;
-    if (M < 1 || M > 16) return NVFP4_ERR_RANGE;
+    if (M < 1 || M > kMaxTokens) return NVFP4_ERR_RANGE;
     if (act != NVFP4_ACT_SILU && act != NVFP4_ACT_GELU_TANH) return NVFP4_ERR_RANGE;
     if (H < 16 || I < 16 || H % 16 != 0 || I % 16 != 0) return NVFP4_ERR_SHAPE;
     if (!aligned16(x) || !aligned16(gate_up_packed) || !aligned16(h) || !aligned16(ws))
@@ -344,10 +379,16 @@ nvfp4_status ffn_gate_up_nvfp4(const void* x, int M, int H, int I, const void* g
     if (need == 0) return NVFP4_ERR_SHAPE;
     if (ws_bytes < need) return NVFP4_ERR_WORKSPACE;
     char* w = reinterpret_cast<char*>(ws);
-    return cuda_status(nvf::launch_stream_gemv(
-        2, x, M, H, gate_up_packed, I, gate_scale2, up_scale2, (int)act, h,
-        reinterpret_cast<int*>(w), reinterpret_cast<int*>(w + nvf::kStatusBytes),
-        w + nvf::kDataOffset, need - nvf::kDataOffset, sms, true, stream));
+    for (int g = 0; g < group_count(M); ++g) {
+        const size_t r0 = (size_t)g * kGroupTokens;
+        const cudaError_t e = nvf::launch_stream_gemv(
+            2, reinterpret_cast<const char*>(x) + r0 * H * 2, group_rows(M, g), H, gate_up_packed,
+            I, gate_scale2, up_scale2, (int)act, reinterpret_cast<char*>(h) + r0 * I * 2,
+            reinterpret_cast<int*>(w), reinterpret_cast<int*>(w + nvf::kStatusBytes),
+            w + nvf::kDataOffset, need - nvf::kDataOffset, sms, true, stream);
+        if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    }
+    return NVFP4_OK;
 }
 
 nvfp4_status nvfp4_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
@@ -388,7 +429,7 @@ const char* nvfp4_status_string(nvfp4_status status) {
         case NVFP4_ERR_NULL: return "null pointer argument";
         case NVFP4_ERR_SHAPE: return "invalid shape (sizes must be positive, K/H/I multiples of 16)";
         case NVFP4_ERR_ALIGN: return "device pointer not 16-byte aligned";
-        case NVFP4_ERR_RANGE: return "argument out of range (M must be 1..16; enum value unknown)";
+        case NVFP4_ERR_RANGE: return "argument out of range (M outside the call's range, or an unknown enum value)";
         case NVFP4_ERR_WORKSPACE: return "workspace too small";
         case NVFP4_ERR_CUDA: return "CUDA runtime error";
         case NVFP4_ERR_TIMEOUT: return "kernel abandoned a bounded wait";

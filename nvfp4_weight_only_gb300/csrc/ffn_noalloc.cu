@@ -62,6 +62,7 @@ extern "C" nvfp4_status ffn_swiglu_nvfp4_noalloc(const void* x, int M, int H, in
     // Every argument check comes first: a rejected call changes nothing.
     const int v = nvf::validate_ffn_args(x, M, H, I, gate_up_packed, down_packed, (int)act, out);
     if (v != NVFP4_OK) return (nvfp4_status)v;
+    if (M > 16) return NVFP4_ERR_RANGE;  // one kernel group: the array is sized for it
     const size_t need = ffn_swiglu_nvfp4_workspace_bytes(M, H, I);
     if (need == 0 || need > kNoAllocWorkspaceBytes) return NVFP4_ERR_WORKSPACE;
     void* ws = nullptr;

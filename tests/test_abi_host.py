@@ -59,7 +59,8 @@ def test_workspace_queries_are_positive(lib):
         assert lib.nvfp4_gemv_workspace_bytes(M, 5120, 17408) > 256
         assert lib.ffn_swiglu_nvfp4_workspace_bytes(M, 5120, 17408) > 256 + M * 17408 * 2
     assert lib.nvfp4_gemv_workspace_bytes(0, 5120, 17408) == 0
-    assert lib.nvfp4_gemv_workspace_bytes(17, 5120, 17408) == 0
+    assert lib.nvfp4_gemv_workspace_bytes(64, 5120, 17408) > 0
+    assert lib.nvfp4_gemv_workspace_bytes(65, 5120, 17408) == 0
     assert lib.nvfp4_quantize_scratch_bytes(5120, 17408) >= 8
 
 
@@ -73,7 +74,7 @@ def test_gemv_validation(lib):
     g = lib.nvfp4_gemv
     assert g(NULL, 1, 64, FAKE, 1.0, 64, FAKE, FAKE, 1 << 20, S) == 1
     assert g(FAKE, 0, 64, FAKE, 1.0, 64, FAKE, FAKE, 1 << 20, S) == 4
-    assert g(FAKE, 17, 64, FAKE, 1.0, 64, FAKE, FAKE, 1 << 20, S) == 4
+    assert g(FAKE, 65, 64, FAKE, 1.0, 64, FAKE, FAKE, 1 << 20, S) == 4
     assert g(FAKE, 1, 40, FAKE, 1.0, 64, FAKE, FAKE, 1 << 20, S) == 2
     assert g(FAKE, 1, 64, FAKE, 1.0, 0, FAKE, FAKE, 1 << 20, S) == 2
     assert g(MISALIGNED, 1, 64, FAKE, 1.0, 64, ctypes.c_void_p(0x20000), FAKE, 1 << 20, S) == 3

@@ -382,7 +382,7 @@ def test_ffn_large_dense_shape(dev, M, act):
 
 
 def test_error_codes_raise(dev):
-    x = torch.zeros(17, 64, dtype=torch.bfloat16, device=dev)
+    x = torch.zeros(65, 64, dtype=torch.bfloat16, device=dev)
     p = torch.zeros(4096, dtype=torch.uint8, device=dev)
     with pytest.raises(ffi.Nvfp4Error) as e:
         ffi.nvfp4_gemv(x, p, 1.0, 64)
@@ -413,3 +413,38 @@ def test_one_workspace_serves_any_sequence_of_shapes(dev):
             ref_y = ffi.nvfp4_gemv(h, dn, q[2][2], H)
             assert torch.equal(ffi.nvfp4_gemv(h, dn, q[2][2], H, ws=shared), ref_y), (M, H, I)
     assert ffi.nvfp4_workspace_status(shared) == 0
+
+
+
+# ------------------------------------------------------------------ M = 17..64
+
+@pytest.mark.parametrize("N,K,M", [(384, 1024, 17), (1000, 2000, 33), (256, 4096, 64),
+                                   (4096, 5120, 24)])
+def test_gemv_large_batches(dev, N, K, M):
+    """M > 16 (verify batches, small prefill): groups of 16 rows and a rest."""
+    run_gemv_case(dev, N, K, M, seed=M + N, outliers=0.01)
+
+
+@pytest.mark.parametrize("M,act", [(17, ffi.NVFP4_ACT_SILU), (40, ffi.NVFP4_ACT_GELU_TANH),
+                                   (64, ffi.NVFP4_ACT_SILU)])
+def test_ffn_large_batches(dev, M, act):
+    run_ffn_case(dev, 512, 1536, M, act, outliers=0.01, seed=M)
+
+
+@pytest.mark.slow
+def test_ffn_large_batch_full_size(dev):
+    run_ffn_case(dev, 5120, 17408, 17, ffi.NVFP4_ACT_SILU, seed=17)
+
+
+def test_large_batch_equals_its_groups_bit_for_bit(dev):
+    """A 37-row call is the 16 + 16 + 5 row calls of its groups."""
+    H, I, M = 512, 1536, 37
+    gu, dn, q, _ = build_ffn(dev, H, I)
+    x = synth.activations_bf16(M, H, seed=4, outlier_frac=0.01).to(dev)
+    full = ffi.ffn_swiglu_nvfp4(x, gu, q[0][2], q[1][2], dn, q[2][2], I)
+    parts = [ffi.ffn_swiglu_nvfp4(x[a:b].contiguous(), gu, q[0][2], q[1][2], dn, q[2][2], I)
+             for a, b in ((0, 16), (16, 32), (32, 37))]
+    assert torch.equal(full, torch.cat(parts))
+    h = ffi.ffn_gate_up_nvfp4(x, gu, q[0][2], q[1][2], I)
+    y = ffi.nvfp4_gemv(h, dn, q[2][2], H)
+    assert torch.equal(y, full)
