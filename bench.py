@@ -548,6 +548,52 @@ def run_sweep(args, ffi, synth, dev, timer, sampler, layers, H, I, peak):
     return res, launches
 
 
+def run_gemv(args):
+    """--gemv N,K: the standalone nvfp4_gemv on enough weight copies (distinct
+    addresses, over 2 GB) that every launch streams from HBM, in one CUDA graph."""
+    import torch
+
+    from nvfp4_weight_only_gb300 import ffi, synth
+
+    N, K = (int(v) for v in args.gemv.split(","))
+    M = args.m or 1
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    ffi.load(build_if_missing=True)
+    w = synth.weights_f32(N, K, seed=N + K, device=dev)
+    c, s, s2 = ffi.nvfp4_quantize(w)
+    del w
+    p = ffi.nvfp4_repack(c, s, N, K)
+    del c, s
+    nbytes = N * K * 0.5625
+    copies = args.layers or int(min(256, max(3, -(-2.2e9 // nbytes))))
+    ps = [p] + [p.clone() for _ in range(copies - 1)]
+    x = synth.activations_bf16(M, K, seed=M, device=dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ws = ffi.workspace(ffi.nvfp4_gemv_workspace_bytes(M, N, K), dev)
+
+    def fn():
+        for pc in ps:
+            ffi.nvfp4_gemv(x, pc, s2, N, ws=ws, out=y)
+
+    timer = GraphTimer(torch.cuda.Stream(device=dev))
+    g = timer.capture(fn)
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    t = timer.time(g, args.steps) / (args.steps * copies)
+    if ffi.nvfp4_workspace_status(ws) != 0:
+        raise RuntimeError("device status word reports a bounded wait abandoned")
+    peak, kind = measured_peaks()
+    gbs = (nbytes + M * K * 2 + M * N * 2) / t / 1e9
+    return {"metric": "µs per standalone nvfp4_gemv launch and effective HBM GB/s",
+            "value": round(gbs, 1), "unit": "GB/s", "us_per_launch": round(t * 1e6, 3),
+            "frac": round(gbs / peak, 4), "peak": peak, "peak_kind": kind, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "config": {"workload": f"standalone GEMV N={N} K={K} M={M}", "copies": copies},
+            "gpu_launches": copies * args.steps}
+
+
 def cpu_baseline(wl, M, budget_s=10.0):
     """The oracle FFN on the host cores for one layer of the workload."""
     import numpy as np
@@ -622,11 +668,16 @@ def main():
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the M=1..16 / other-shape sweep (one GPU only)")
     ap.add_argument("--sweep-reps", type=int, default=10)
+    ap.add_argument("--gemv", default=None, metavar="N,K",
+                    help="time the standalone GEMV of one N x K projection instead")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     wl = WORKLOADS[args.workload]
+    if args.gemv:
+        print(json.dumps(run_gemv(args)), flush=True)
+        return
     if args.impl == "reference":
         line = run_reference(args, wl)
     else:
