@@ -234,7 +234,8 @@ nvfp4_status ffn_swiglu_nvfp4_lora(const void* x, int M, int H, int I,
                                    const void* up_b, const void* down_a, const void* down_b,
                                    void* out, void* ws, size_t ws_bytes, cudaStream_t stream);
 
-/* Scratch bytes for nvfp4_lora_apply (the bf16 xa [M, r]). */
+/* Scratch bytes for nvfp4_lora_apply (fp32 partial sums of a v over K slices;
+ * independent of K). */
 size_t nvfp4_lora_apply_scratch_bytes(int M, int rank);
 
 /*

@@ -241,8 +241,9 @@ nvfp4_status ffn_swiglu_nvfp4(const void* x, int M, int H, int I, const void* ga
     return NVFP4_OK;
 }
 
-// LoRA FFN workspace: the FFN's, then xa_gate [M, r], xa_up [M, r], the gate
-// and up deltas [M, I] each, and xa_down [M, r] (all bf16).
+// LoRA FFN workspace: the FFN's, then the fp32 slice sums of A_gate x, A_up x
+// (lora_partial_bytes each), the bf16 gate and up deltas [M, I] each, and the
+// slice sums of A_down h.
 struct LoraLayout {
     FfnLayout ffn;
     size_t xa_g, xa_u, d_g, d_u, xa_d, total;
@@ -251,7 +252,7 @@ struct LoraLayout {
 LoraLayout lora_layout(int M, int H, int I, int r, int sms) {
     LoraLayout l;
     l.ffn = ffn_layout(M, H, I, sms);
-    const size_t xr = round256((size_t)M * r * 2), xi = round256((size_t)M * I * 2);
+    const size_t xr = round256(nvf::lora_partial_bytes(M, r)), xi = round256((size_t)M * I * 2);
     l.xa_g = l.ffn.total;
     l.xa_u = l.xa_g + xr;
     l.d_g = l.xa_u + xr;
@@ -313,7 +314,7 @@ nvfp4_status ffn_swiglu_nvfp4_lora(const void* x, int M, int H, int I, const voi
     if (np > 0) {
         e = nvf::launch_lora_xa(x, M, H, A, xa, np, rank, stream);
         if (e != cudaSuccess) return NVFP4_ERR_CUDA;
-        e = nvf::launch_lora_delta(xa, B, d, np, M, I, rank, false, stream);
+        e = nvf::launch_lora_delta(xa, H, B, d, np, M, I, rank, false, stream);
         if (e != cudaSuccess) return NVFP4_ERR_CUDA;
     }
     e = nvf::launch_stream_gemv(2, x, M, H, gate_up_packed, I, gate_scale2, up_scale2, (int)act, h,
@@ -331,7 +332,7 @@ nvfp4_status ffn_swiglu_nvfp4_lora(const void* x, int M, int H, int I, const voi
     if (e != cudaSuccess) return NVFP4_ERR_CUDA;
     if (down_a) {  // out = bf16(out + B_down xa_down)
         const void* xac = xad;
-        e = nvf::launch_lora_delta(&xac, &down_b, &out, 1, M, H, rank, true, stream);
+        e = nvf::launch_lora_delta(&xac, I, &down_b, &out, 1, M, H, rank, true, stream);
         if (e != cudaSuccess) return NVFP4_ERR_CUDA;
     }
     return NVFP4_OK;
@@ -339,7 +340,7 @@ nvfp4_status ffn_swiglu_nvfp4_lora(const void* x, int M, int H, int I, const voi
 
 size_t nvfp4_lora_apply_scratch_bytes(int M, int rank) {
     if (M < 1 || M > 16 || rank < 1 || rank > nvf::kLoraMaxRank) return 0;
-    return round256((size_t)M * rank * 2);
+    return round256(nvf::lora_partial_bytes(M, rank));
 }
 
 nvfp4_status nvfp4_lora_apply(const void* v, int M, int K, const void* a, const void* b, int rank,
@@ -355,7 +356,7 @@ nvfp4_status nvfp4_lora_apply(const void* v, int M, int K, const void* a, const 
     cudaError_t e = nvf::launch_lora_xa(v, M, K, &a, &scratch, 1, rank, stream);
     if (e != cudaSuccess) return NVFP4_ERR_CUDA;
     const void* xa = scratch;
-    return cuda_status(nvf::launch_lora_delta(&xa, &b, &base, 1, M, N, rank, true, stream));
+    return cuda_status(nvf::launch_lora_delta(&xa, K, &b, &base, 1, M, N, rank, true, stream));
 }
 
 size_t ffn_gate_up_nvfp4_workspace_bytes(int M, int H, int I) {

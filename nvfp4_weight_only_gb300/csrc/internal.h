@@ -42,13 +42,21 @@ int device_sm_count();
 
 // lora.cu: the adapter overlay, dW = B A (A [r, K], B [N, r], bf16).
 constexpr int kLoraMaxRank = 64;
-// xa[p] [M, r] = bf16(A[p] v) for each of `pairs` (1 or 2) matrices A[p] [r, K].
-cudaError_t launch_lora_xa(const void* v, int M, int K, const void* const* A, void* const* xa,
+constexpr int kLoraMaxSplit = 32;  // K slices of the A v partial sums
+// Slices the A v sums over K take (the same for both launches below).
+int lora_split(int K);
+// fp32 bytes of one pair's partial sums [r][split][M] (split at its maximum).
+size_t lora_partial_bytes(int M, int r);
+// part[p] = per-slice fp32 sums of A[p] v for each of `pairs` (1 or 2)
+// matrices A[p] [r, K]; v is [M, K].
+cudaError_t launch_lora_xa(const void* v, int M, int K, const void* const* A, void* const* part,
                            int pairs, int r, cudaStream_t s);
-// d = bf16(B[p] xa[p]) [M, N]: stored in out[p] (add false) or added to it as
+// xa = bf16(sum of the slices of part[p]) (K as given to launch_lora_xa), then
+// d = bf16(B[p] xa) [M, N]: stored in out[p] (add false) or added to it as
 // out[p] = bf16(out[p] + d) (add true).
-cudaError_t launch_lora_delta(const void* const* xa, const void* const* B, void* const* out,
-                              int pairs, int M, int N, int r, bool add, cudaStream_t s);
+cudaError_t launch_lora_delta(const void* const* part, int K, const void* const* B,
+                              void* const* out, int pairs, int M, int N, int r, bool add,
+                              cudaStream_t s);
 
 // Whether the kernel's shared-memory plan for this problem has the alignment
 // its accesses assume (the launcher refuses plans that do not).

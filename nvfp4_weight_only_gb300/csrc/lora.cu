@@ -3,12 +3,16 @@
 // up take dW x before the activation, the output takes dW h after the down
 // projection), dW = B A with A [r, in] and B [out, r] in bf16.
 //
-//   lora_xa_kernel:    xa[m][j]   = bf16(sum_k A[j][k] v[m][k])        (A v)
-//   lora_delta_kernel: d[m][n]    = bf16(sum_j B[n][j] xa[m][j])       (B xa)
-//                      and either stores d or base[m][n] = bf16(base + d)
+//   lora_xa_partial_kernel: part[j][s][m] = sum over K slice s of A[j][k] v[m][k]
+//   lora_delta_kernel:      xa[m][j] = bf16(sum_s part[j][s][m])         (A v)
+//                           d[m][n]  = bf16(sum_j B[n][j] xa[m][j])      (B xa)
+//                           then stores d or base[m][n] = bf16(base + d)
 //
 // Both are small next to the FFN's weight stream (r rows of A, r columns of
-// B); they sum in a fixed order, so results are deterministic.
+// B), so what costs time is latency: the K sum is cut into slices that each
+// CTA covers with one vector load per thread, and every thread issues all of
+// its loads before the first multiply.  Sums run in a fixed order, so results
+// are deterministic.
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -20,114 +24,204 @@ namespace nvf {
 constexpr int kLoraThreads = 256;
 constexpr int kLoraMaxM = 16;
 
+int lora_split(int K) {
+    const int kv = (K % 8 == 0) ? K / 8 : K / 2;  // vectors of the partial kernel
+    const int s = (kv + kLoraThreads - 1) / kLoraThreads;
+    return s < 1 ? 1 : (s > kLoraMaxSplit ? kLoraMaxSplit : s);
+}
+
+size_t lora_partial_bytes(int M, int r) {
+    return (size_t)M * r * kLoraMaxSplit * sizeof(float);
+}
+
 struct LoraXaArgs {
     const __nv_bfloat16* v;  // [M, K]
     const __nv_bfloat16* A[2];
-    __nv_bfloat16* xa[2];    // [M, r]
-    int M, K, r;
+    float* part[2];          // [r][split][M]
+    int M, K, split;
 };
 
-// One block per (row j of A, pair): every thread accumulates its K stride for
-// all M tokens in fp32, then the block sums in a fixed order (warp butterfly,
-// then the warps in index order).
-__global__ void __launch_bounds__(kLoraThreads) lora_xa_kernel(const LoraXaArgs a) {
-    const int j = blockIdx.x, p = blockIdx.y;
+template <typename Vec>
+__device__ __forceinline__ float dot_acc(const Vec& w, const Vec& x, float acc) {
+    constexpr int kPairs = sizeof(Vec) / 4;
+    const uint32_t* wp = reinterpret_cast<const uint32_t*>(&w);
+    const uint32_t* xp = reinterpret_cast<const uint32_t*>(&x);
+#pragma unroll
+    for (int i = 0; i < kPairs; ++i) {
+        __nv_bfloat162 wb, xb;
+        *reinterpret_cast<uint32_t*>(&wb) = wp[i];
+        *reinterpret_cast<uint32_t*>(&xb) = xp[i];
+        const float2 wf = __bfloat1622float2(wb), xf = __bfloat1622float2(xb);
+        acc = fmaf(wf.x, xf.x, acc);
+        acc = fmaf(wf.y, xf.y, acc);
+    }
+    return acc;
+}
+
+// One block per (K slice s, row j of A, pair p).  Vec is uint4 (8 bf16) when
+// K % 8 == 0, else uint32_t (2 bf16).  A thread loads its A vector and the M
+// matching token vectors together, then multiplies; the block sums each token
+// in a fixed order (warp butterfly, then the warps in index order).
+template <typename Vec>
+__global__ void __launch_bounds__(kLoraThreads) lora_xa_partial_kernel(const LoraXaArgs a) {
+    constexpr int kElems = sizeof(Vec) / 2;
+    const int s = blockIdx.x, j = blockIdx.y, p = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const __nv_bfloat162* arow = reinterpret_cast<const __nv_bfloat162*>(a.A[p] + (size_t)j * a.K);
+    const int kv = a.K / kElems;
+    const int per = (kv + a.split - 1) / a.split;
+    const int v0 = s * per;
+    const int v1 = min(kv, v0 + per);
+    const __nv_bfloat16* A = p ? a.A[1] : a.A[0];  // no dynamic index into the parameters
+    const Vec* arow = reinterpret_cast<const Vec*>(A + (size_t)j * a.K);
     float acc[kLoraMaxM];
 #pragma unroll
     for (int m = 0; m < kLoraMaxM; ++m) acc[m] = 0.0f;
-    const int K2 = a.K / 2;
-    for (int k2 = tid; k2 < K2; k2 += kLoraThreads) {
-        const float2 w = __bfloat1622float2(arow[k2]);
+    for (int i = v0 + tid; i < v1; i += kLoraThreads) {
+        const Vec w = arow[i];
+        Vec xv[kLoraMaxM];
 #pragma unroll
-        for (int m = 0; m < kLoraMaxM; ++m) {
-            if (m < a.M) {
-                const float2 x = __bfloat1622float2(
-                    reinterpret_cast<const __nv_bfloat162*>(a.v + (size_t)m * a.K)[k2]);
-                acc[m] = fmaf(w.x, x.x, acc[m]);
-                acc[m] = fmaf(w.y, x.y, acc[m]);
-            }
-        }
+        for (int m = 0; m < kLoraMaxM; ++m)
+            if (m < a.M) xv[m] = reinterpret_cast<const Vec*>(a.v + (size_t)m * a.K)[i];
+#pragma unroll
+        for (int m = 0; m < kLoraMaxM; ++m)
+            if (m < a.M) acc[m] = dot_acc(w, xv[m], acc[m]);
     }
     __shared__ float red[kLoraThreads / 32][kLoraMaxM];
 #pragma unroll
     for (int m = 0; m < kLoraMaxM; ++m) {
-        float s = acc[m];
+        if (m < a.M) {
+            float t = acc[m];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        if (lane == 0) red[warp][m] = s;
+            for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+            if (lane == 0) red[warp][m] = t;
+        }
     }
     __syncthreads();
     if (tid < a.M) {
-        float s = 0.0f;
+        float t = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kLoraThreads / 32; ++w) s += red[w][tid];
-        a.xa[p][(size_t)tid * a.r + j] = __float2bfloat16_rn(s);
+        for (int w = 0; w < kLoraThreads / 32; ++w) t += red[w][tid];
+        (p ? a.part[1] : a.part[0])[((size_t)j * a.split + s) * a.M + tid] = t;
     }
 }
 
 struct LoraDeltaArgs {
-    const __nv_bfloat16* xa[2];  // [M, r]
+    const float* part[2];        // [r][split][M]
     const __nv_bfloat16* B[2];   // [N, r]
     __nv_bfloat16* out[2];       // [M, N]: the delta, or the base it is added to
-    int M, N, r, add;
+    int M, N, r, split, add;
 };
 
-// One thread per output row n: d = bf16(sum_j B[n][j] xa[m][j]) for every m,
-// then stored (add == 0) or added to the base as bf16(base + d).  A bf16 plus
-// a bf16 is exact in fp32 whenever the smaller term can move the rounding, so
-// one rounding of the fp32 sum is the bf16 rounding of the exact sum.
+// One thread per output row n.  The block first completes xa = bf16(sum of the
+// slice partials, in slice order) into shared memory; each thread then loads
+// its whole B row before multiplying, forms d = bf16(sum_j B[n][j] xa[m][j])
+// for every m and stores it (add == 0) or adds it to the base as
+// bf16(base + d).  A bf16 plus a bf16 is exact in fp32 whenever the smaller
+// term can move the rounding, so one rounding of the fp32 sum is the bf16
+// rounding of the exact sum.
+template <bool kVec>
 __global__ void __launch_bounds__(kLoraThreads) lora_delta_kernel(const LoraDeltaArgs a) {
     const int p = blockIdx.y;
-    __shared__ float xs[kLoraMaxM * 64];
-    for (int i = threadIdx.x; i < a.M * a.r; i += kLoraThreads)
-        xs[i] = __bfloat162float(a.xa[p][i]);
+    __shared__ float xs[kLoraMaxM * kLoraMaxRank];  // [m][j]
+    for (int i = threadIdx.x; i < a.M * a.r; i += kLoraThreads) {
+        const int m = i / a.r, j = i - m * a.r;
+        const float* q = (p ? a.part[1] : a.part[0]) + (size_t)j * a.split * a.M + m;
+        float t = 0.0f;
+        for (int sl = 0; sl < a.split; ++sl) t += q[(size_t)sl * a.M];
+        xs[i] = __bfloat162float(__float2bfloat16_rn(t));
+    }
     __syncthreads();
     const int n = blockIdx.x * kLoraThreads + threadIdx.x;
     if (n >= a.N) return;
-    const __nv_bfloat16* brow = a.B[p] + (size_t)n * a.r;
-    for (int m = 0; m < a.M; ++m) {
-        float s = 0.0f;
-        for (int j = 0; j < a.r; ++j) s = fmaf(__bfloat162float(brow[j]), xs[m * a.r + j], s);
-        const __nv_bfloat16 d = __float2bfloat16_rn(s);
-        __nv_bfloat16* o = a.out[p] + (size_t)m * a.N + n;
-        *o = a.add ? __float2bfloat16_rn(__bfloat162float(*o) + __bfloat162float(d)) : d;
+    float acc[kLoraMaxM];
+#pragma unroll
+    for (int m = 0; m < kLoraMaxM; ++m) acc[m] = 0.0f;
+    const __nv_bfloat16* brow = (p ? a.B[1] : a.B[0]) + (size_t)n * a.r;
+    if (kVec) {  // r % 8 == 0: at most 8 16-byte loads, all issued first
+        constexpr int kMaxV = kLoraMaxRank / 8;
+        const int nv = a.r / 8;
+        uint4 bv[kMaxV];
+#pragma unroll
+        for (int c = 0; c < kMaxV; ++c)
+            if (c < nv) bv[c] = reinterpret_cast<const uint4*>(brow)[c];
+#pragma unroll
+        for (int c = 0; c < kMaxV; ++c) {
+            if (c < nv) {
+                const uint32_t words[4] = {bv[c].x, bv[c].y, bv[c].z, bv[c].w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t wd = words[e >> 1];  // element 2i in the low half
+                    const float bj = __uint_as_float((e & 1) ? (wd & 0xffff0000u) : (wd << 16));
+                    const int j = 8 * c + e;
+#pragma unroll
+                    for (int m = 0; m < kLoraMaxM; ++m)
+                        if (m < a.M) acc[m] = fmaf(bj, xs[m * a.r + j], acc[m]);
+                }
+            }
+        }
+    } else {
+#pragma unroll 8
+        for (int j = 0; j < a.r; ++j) {
+            const float bj = __bfloat162float(brow[j]);
+#pragma unroll
+            for (int m = 0; m < kLoraMaxM; ++m)
+                if (m < a.M) acc[m] = fmaf(bj, xs[m * a.r + j], acc[m]);
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < kLoraMaxM; ++m) {
+        if (m < a.M) {
+            const __nv_bfloat16 d = __float2bfloat16_rn(acc[m]);
+            __nv_bfloat16* o = (p ? a.out[1] : a.out[0]) + (size_t)m * a.N + n;
+            *o = a.add ? __float2bfloat16_rn(__bfloat162float(*o) + __bfloat162float(d)) : d;
+        }
     }
 }
 
-cudaError_t launch_lora_xa(const void* v, int M, int K, const void* const* A, void* const* xa,
+cudaError_t launch_lora_xa(const void* v, int M, int K, const void* const* A, void* const* part,
                            int pairs, int r, cudaStream_t s) {
-    if (M < 1 || M > kLoraMaxM || r < 1 || r > kLoraMaxRank || pairs < 1 || pairs > 2 || K % 2)
+    if (M < 1 || M > kLoraMaxM || r < 1 || r > kLoraMaxRank || pairs < 1 || pairs > 2 || K < 2 ||
+        K % 2)
         return cudaErrorInvalidValue;
     LoraXaArgs a{};
     a.v = reinterpret_cast<const __nv_bfloat16*>(v);
     for (int p = 0; p < pairs; ++p) {
         a.A[p] = reinterpret_cast<const __nv_bfloat16*>(A[p]);
-        a.xa[p] = reinterpret_cast<__nv_bfloat16*>(xa[p]);
+        a.part[p] = reinterpret_cast<float*>(part[p]);
     }
     a.M = M;
     a.K = K;
-    a.r = r;
-    lora_xa_kernel<<<dim3(r, pairs), kLoraThreads, 0, s>>>(a);
+    a.split = lora_split(K);
+    const dim3 grid(a.split, r, pairs);
+    if (K % 8 == 0)
+        lora_xa_partial_kernel<uint4><<<grid, kLoraThreads, 0, s>>>(a);
+    else
+        lora_xa_partial_kernel<uint32_t><<<grid, kLoraThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_lora_delta(const void* const* xa, const void* const* B, void* const* out,
-                              int pairs, int M, int N, int r, bool add, cudaStream_t s) {
-    if (M < 1 || M > kLoraMaxM || r < 1 || r > kLoraMaxRank || pairs < 1 || pairs > 2 || N < 1)
+cudaError_t launch_lora_delta(const void* const* part, int K, const void* const* B,
+                              void* const* out, int pairs, int M, int N, int r, bool add,
+                              cudaStream_t s) {
+    if (M < 1 || M > kLoraMaxM || r < 1 || r > kLoraMaxRank || pairs < 1 || pairs > 2 || N < 1 ||
+        K < 2)
         return cudaErrorInvalidValue;
     LoraDeltaArgs a{};
     for (int p = 0; p < pairs; ++p) {
-        a.xa[p] = reinterpret_cast<const __nv_bfloat16*>(xa[p]);
+        a.part[p] = reinterpret_cast<const float*>(part[p]);
         a.B[p] = reinterpret_cast<const __nv_bfloat16*>(B[p]);
         a.out[p] = reinterpret_cast<__nv_bfloat16*>(out[p]);
     }
     a.M = M;
     a.N = N;
     a.r = r;
+    a.split = lora_split(K);
     a.add = add ? 1 : 0;
-    lora_delta_kernel<<<dim3((N + kLoraThreads - 1) / kLoraThreads, pairs), kLoraThreads, 0, s>>>(a);
+    const dim3 grid((N + kLoraThreads - 1) / kLoraThreads, pairs);
+    if (r % 8 == 0)
+        lora_delta_kernel<true><<<grid, kLoraThreads, 0, s>>>(a);
+    else
+        lora_delta_kernel<false><<<grid, kLoraThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

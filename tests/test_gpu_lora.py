@@ -118,7 +118,9 @@ def test_lora_zero_b_is_the_plain_ffn_bit_for_bit(dev):
     assert torch.equal(again, plain)
 
 
-@pytest.mark.parametrize("M,K,N,r", [(1, 5120, 17408, 16), (5, 4096, 300, 64), (16, 512, 64, 3)])
+@pytest.mark.parametrize("M,K,N,r", [(1, 5120, 17408, 16), (5, 4096, 300, 64), (16, 512, 64, 3),
+                                     (2, 1030, 100, 8),      # K % 8 != 0: 4-byte vectors
+                                     (3, 70000, 64, 24)])    # more K slices than the cap
 def test_lora_apply_standalone(dev, M, K, N, r):
     v = _bf16((M, K), 3, 1.0)
     a = _bf16((r, K), 4, 0.05)
