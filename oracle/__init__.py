@@ -75,6 +75,18 @@ def lib():
                                    u8p, u8p, ctypes.c_float, u8p, u8p, ctypes.c_float,
                                    ctypes.c_int, i64, vp, vp, vp, vp, vp, vp, u16p, u16p]
         L.orc_ffn_lora.restype = None
+        L.orc_fp8_dequantize.argtypes = [u8p, f32p, i64, i64, f64p]
+        L.orc_fp8_dequantize.restype = None
+        L.orc_gemv_fp8_f64.argtypes = [u16p, i64, i64, u8p, f32p, i64, f64p]
+        L.orc_gemv_fp8_f64.restype = None
+        L.orc_gemv_fp8.argtypes = [u16p, i64, i64, u8p, f32p, i64, u16p]
+        L.orc_gemv_fp8.restype = None
+        L.orc_ffn_fp8_hidden.argtypes = [u16p, i64, i64, i64, u8p, f32p, u8p, f32p, ctypes.c_int,
+                                         u16p]
+        L.orc_ffn_fp8_hidden.restype = None
+        L.orc_ffn_fp8.argtypes = [u16p, i64, i64, i64, u8p, f32p, u8p, f32p, u8p, f32p,
+                                  ctypes.c_int, u16p]
+        L.orc_ffn_fp8.restype = None
         L.orc_set_threads.argtypes = [ctypes.c_int]
         L.orc_set_threads.restype = ctypes.c_int
         _lib = L
@@ -290,3 +302,66 @@ def ffn_lora(x_bits, I, gate, up, down, act=ACT_SILU, lora=None):
                        ptr(lora.get("up"), 0), ptr(lora.get("up"), 1),
                        ptr(lora.get("down"), 0), ptr(lora.get("down"), 1), out, h)
     return out, h
+
+
+# ---------------------------------------------------------------- block-scaled FP8
+
+def fp8_grid_shape(N, K):
+    """Shape of the FP32 block-scale grid of an FP8 projection [N, K]."""
+    return (N + 127) // 128, (K + 127) // 128
+
+
+def fp8_dequantize(q, bs):
+    """E4M3 bytes [N, K] and FP32 grid -> weights [N, K] (float64)."""
+    q = _c(q, np.uint8)
+    N, K = q.shape
+    assert tuple(np.shape(bs)) == fp8_grid_shape(N, K)
+    w = np.zeros((N, K), np.float64)
+    lib().orc_fp8_dequantize(q, _c(bs, np.float32), N, K, w)
+    return w
+
+
+def gemv_fp8_f64(x_bits, q, bs):
+    x = _c(x_bits, np.uint16)
+    q = _c(q, np.uint8)
+    M, K = x.shape
+    N = q.shape[0]
+    assert q.shape[1] == K and tuple(np.shape(bs)) == fp8_grid_shape(N, K)
+    y = np.zeros((M, N), np.float64)
+    lib().orc_gemv_fp8_f64(x, M, K, q, _c(bs, np.float32), N, y)
+    return y
+
+
+def gemv_fp8(x_bits, q, bs):
+    """bf16 bits [M, K] x FP8 projection (q [N, K], grid) -> bf16 bits [M, N]."""
+    x = _c(x_bits, np.uint16)
+    q = _c(q, np.uint8)
+    M, K = x.shape
+    N = q.shape[0]
+    assert q.shape[1] == K and tuple(np.shape(bs)) == fp8_grid_shape(N, K)
+    y = np.zeros((M, N), np.uint16)
+    lib().orc_gemv_fp8(x, M, K, q, _c(bs, np.float32), N, y)
+    return y
+
+
+def ffn_fp8_hidden(x_bits, gate, up, act=ACT_SILU):
+    """gate/up = (q [I, H], grid).  Returns h bf16 bits [M, I]."""
+    x = _c(x_bits, np.uint16)
+    M, H = x.shape
+    I = gate[0].shape[0]
+    h = np.zeros((M, I), np.uint16)
+    lib().orc_ffn_fp8_hidden(x, M, H, I, _c(gate[0], np.uint8), _c(gate[1], np.float32),
+                             _c(up[0], np.uint8), _c(up[1], np.float32), int(act), h)
+    return h
+
+
+def ffn_fp8(x_bits, gate, up, down, act=ACT_SILU):
+    """Full FP8 FFN; returns out bf16 bits [M, H]."""
+    x = _c(x_bits, np.uint16)
+    M, H = x.shape
+    I = gate[0].shape[0]
+    out = np.zeros((M, H), np.uint16)
+    lib().orc_ffn_fp8(x, M, H, I, _c(gate[0], np.uint8), _c(gate[1], np.float32),
+                      _c(up[0], np.uint8), _c(up[1], np.float32),
+                      _c(down[0], np.uint8), _c(down[1], np.float32), int(act), out)
+    return out

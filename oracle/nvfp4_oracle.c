@@ -354,6 +354,99 @@ void orc_ffn(const uint16_t *x, int64_t M, int64_t H, int64_t I,
     free(h);
 }
 
+/* ---------------- block-scaled FP8 (w8a16) ---------------- */
+
+/*
+ * The dense-FFN page's native FP8 arm ("spark_model/layers/dense_ffn.rs",
+ * DenseFfnWeightsFp8 and the FP8 dispatch of DenseFfnLayer::forward: a dual
+ * gate/up GEMV, then the activation-consuming down GEMV; the weight loader's
+ * proj_is_fp8_any_scale): a projection is E4M3 bytes q [N, K] row-major plus
+ * an FP32 grid bs [ceil(N/128), ceil(K/128)] row-major, and
+ *     W[n][k] = e4m3(q[n][k]) * bs[n/128][k/128]
+ * with no per-tensor scale (a per-tensor scalar is the uniform grid).
+ * Reading: the roundings are those of the NVFP4 path (gate_out, up_out and
+ * the activation product are bf16 buffers on the same page).
+ */
+
+static double fp8_weight(const uint8_t *q, const float *bs, int64_t K, int64_t n, int64_t k)
+{
+    const int64_t kb = (K + 127) / 128;
+    return orc_e4m3_decode(q[n * K + k]) * (double)bs[(n / 128) * kb + k / 128];
+}
+
+/* Dequantised weight [N, K] in double. */
+void orc_fp8_dequantize(const uint8_t *q, const float *bs, int64_t N, int64_t K, double *w)
+{
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            w[n * K + k] = fp8_weight(q, bs, K, n, k);
+}
+
+/* y[m, n] = sum_k x[m, k] * W[n][k] in double, before the bf16 rounding. */
+void orc_gemv_fp8_f64(const uint16_t *x, int64_t M, int64_t K, const uint8_t *q,
+                      const float *bs, int64_t N, double *y)
+{
+    int64_t n;
+#pragma omp parallel for schedule(static)
+    for (n = 0; n < N; ++n) {
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += orc_bf16_decode(x[m * K + k]) * fp8_weight(q, bs, K, n, k);
+            y[m * N + n] = acc;
+        }
+    }
+}
+
+/* The FP8 GEMV with its bf16 output rounding: y bf16 [M, N]. */
+void orc_gemv_fp8(const uint16_t *x, int64_t M, int64_t K, const uint8_t *q, const float *bs,
+                  int64_t N, uint16_t *y)
+{
+    double *t = (double *)malloc((size_t)(M * N > 0 ? M * N : 1) * sizeof(double));
+    if (!t)
+        return;
+    orc_gemv_fp8_f64(x, M, K, q, bs, N, t);
+    for (int64_t i = 0; i < M * N; ++i)
+        y[i] = orc_bf16_from_double(t[i]);
+    free(t);
+}
+
+/* h[m, i] = bf16(act(g) * u) from the bf16 projections of the FP8 gate and up. */
+void orc_ffn_fp8_hidden(const uint16_t *x, int64_t M, int64_t H, int64_t I, const uint8_t *gq,
+                        const float *gbs, const uint8_t *uq, const float *ubs, int act,
+                        uint16_t *h)
+{
+    uint16_t *g = (uint16_t *)malloc((size_t)(M * I > 0 ? M * I : 1) * 2);
+    uint16_t *u = (uint16_t *)malloc((size_t)(M * I > 0 ? M * I : 1) * 2);
+    if (!g || !u) {
+        free(g);
+        free(u);
+        return;
+    }
+    orc_gemv_fp8(x, M, H, gq, gbs, I, g);
+    orc_gemv_fp8(x, M, H, uq, ubs, I, u);
+    for (int64_t i = 0; i < M * I; ++i) {
+        double gv = orc_bf16_decode(g[i]), uv = orc_bf16_decode(u[i]);
+        double a = (act == 0) ? orc_silu(gv) : orc_gelu_tanh(gv);
+        h[i] = orc_bf16_from_double(a * uv);
+    }
+    free(g);
+    free(u);
+}
+
+/* Full FP8 FFN: out bf16 [M, H] = bf16(down(h)). */
+void orc_ffn_fp8(const uint16_t *x, int64_t M, int64_t H, int64_t I, const uint8_t *gq,
+                 const float *gbs, const uint8_t *uq, const float *ubs, const uint8_t *dq,
+                 const float *dbs, int act, uint16_t *out)
+{
+    uint16_t *h = (uint16_t *)malloc((size_t)(M * I > 0 ? M * I : 1) * 2);
+    if (!h)
+        return;
+    orc_ffn_fp8_hidden(x, M, H, I, gq, gbs, uq, ubs, act, h);
+    orc_gemv_fp8(h, M, I, dq, dbs, H, out);
+    free(h);
+}
+
 /* ---------------- LoRA overlay ---------------- */
 
 /*
