@@ -45,7 +45,8 @@ WORKLOADS = {
                   desc="large dense FFN H=5376 I=21504 M=1..16 SiLU, 62 layers"),
 }
 
-KERNEL_SOURCES = ["nvfp4_weight_only_gb300/csrc/stream_gemv.cu",
+KERNEL_SOURCES = ["nvfp4_weight_only_gb300/csrc/stream_kernel.cuh",
+                  "nvfp4_weight_only_gb300/csrc/stream_gemv.cu",
                   "nvfp4_weight_only_gb300/csrc/device_util.cuh",
                   "nvfp4_weight_only_gb300/csrc/layout.h"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dual_gate_up_single_token_traffic.json")
@@ -62,6 +63,89 @@ def dual_kernel_bytes(H, I, M):
 
 def down_kernel_bytes(H, I, M):
     return H * I * 0.5625 + M * I * 2 + M * H * 2
+
+
+def grid_bytes(N, K):
+    return ((N + 127) // 128) * ((K + 127) // 128) * 4
+
+
+def w8a16_layer_bytes(H, I, M):
+    # FP8 codes and block grids of gate, up and down, x read, out written
+    return 3 * H * I + 2 * grid_bytes(I, H) + grid_bytes(H, I) + 2 * M * H * 2
+
+
+def w8a16_dual_bytes(H, I, M):
+    return 2 * H * I + 2 * grid_bytes(I, H) + M * H * 2 + M * I * 2
+
+
+def w8a16_down_bytes(H, I, M):
+    return H * I + grid_bytes(H, I) + M * I * 2 + M * H * 2
+
+
+def build_w8a16_layers(ffi, synth, H, I, L, dev):
+    """L distinct block-scaled FP8 FFN layers (seeded stand-ins for an FP8
+    checkpoint), repacked on the device (load time, untimed)."""
+    import torch
+
+    layers = []
+    for li in range(L):
+        proj = [synth.fp8_weights(n, k, seed=synth.layer_seed(li, p) + 77, device=dev)
+                for p, (n, k) in ((synth.GATE, (I, H)), (synth.UP, (I, H)), (synth.DOWN, (H, I)))]
+        gu = ffi.w8a16_repack_gate_up(proj[0][0], proj[0][1], proj[1][0], proj[1][1])
+        dn = ffi.w8a16_repack(*proj[2])
+        layers.append((gu, dn))
+        del proj
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return layers
+
+
+def w8a16_case(ffi, synth, timer, dev, lyrs, H, I, M, act, reps, peak, kernels=True):
+    """µs per layer of ffn_swiglu_w8a16 over the distinct layers in one CUDA
+    graph, and (kernels) each of its two kernels alone.  Returns (entry,
+    launches, wall-clock window)."""
+    import torch
+
+    x = synth.activations_bf16(M, H, seed=M, device=dev)
+    out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    L = ffi.load()
+    ws = ffi.workspace(L.ffn_swiglu_w8a16_workspace_bytes(M, H, I), dev)
+
+    def fn():
+        for gu, dn in lyrs:
+            ffi.ffn_swiglu_w8a16(x, gu, dn, I, act, ws=ws, out=out)
+
+    g = timer.capture(fn)
+    w0 = time.time()
+    t = timer.time(g, reps, warmup=3) / (reps * len(lyrs))
+    launches = 2 * len(lyrs) * reps
+    gbs = w8a16_layer_bytes(H, I, M) / t / 1e9
+    entry = {"us_per_layer": round(t * 1e6, 3), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    del g
+    if kernels:
+        # the down kernel alone through w8a16_gemv; the gate/up kernel is the
+        # layer minus it (the two run back to back in the FFN)
+        h = synth.activations_bf16(M, I, seed=M + 1, device=dev)
+        ws_g = ffi.workspace(L.w8a16_gemv_workspace_bytes(M, H, I), dev)
+
+        def down():
+            for gu, dn in lyrs:
+                ffi.w8a16_gemv(h, dn, H, ws=ws_g, out=out)
+
+        gk = timer.capture(down)
+        tk = timer.time(gk, reps, warmup=3) / (reps * len(lyrs))
+        launches += len(lyrs) * reps
+        del gk
+        entry["down"] = {"us_per_launch": round(tk * 1e6, 3),
+                         "frac": round(w8a16_down_bytes(H, I, M) / tk / 1e9 / peak, 4)}
+        td = t - tk  # the layer is the two kernels back to back
+        entry["dual"] = {"us_per_launch": round(td * 1e6, 3), "derived": "layer minus down",
+                         "frac": round(w8a16_dual_bytes(H, I, M) / td / 1e9 / peak, 4)}
+        if ffi.nvfp4_workspace_status(ws_g) != 0:
+            raise RuntimeError("device status word reports a bounded wait abandoned")
+    if ffi.nvfp4_workspace_status(ws) != 0:
+        raise RuntimeError("device status word reports a bounded wait abandoned")
+    return entry, launches, (w0, time.time())
 
 
 def kernel_source_hash():
@@ -502,6 +586,18 @@ def run_sweep(args, ffi, synth, dev, timer, sampler, layers, H, I, peak):
     res[f"ffn_{H}x{I}_lora_gate_up_down"] = lr
     torch.cuda.empty_cache()
 
+    # block-scaled FP8 weights (the pages' native FP8 arm) on the headline layer
+    f8 = {}
+    f8_layers = build_w8a16_layers(ffi, synth, H, I, 24, dev)
+    for M in (1, 2, 4, 8, 16):
+        entry, n, win = w8a16_case(ffi, synth, timer, dev, f8_layers, H, I, M, 0, reps, peak)
+        launches += n
+        sampler.mark(*win)
+        f8[f"M{M}"] = entry
+    res[f"ffn_{H}x{I}_w8a16_silu"] = f8
+    del f8_layers
+    torch.cuda.empty_cache()
+
     for key, Hs, Is, Ls, Ms in (("spec_verify", 4096, 12288, 32, (2, 3)),
                                 ("large", 5376, 21504, 62, (1, 2, 4, 8, 12, 16))):
         lyrs = build_layers(ffi, synth, Hs, Is, Ls, dev)
@@ -594,6 +690,30 @@ def run_gemv(args):
             "gpu_launches": copies * args.steps}
 
 
+def run_w8a16(args):
+    """--w8a16: the block-scaled FP8 FFN on the headline layer (5120 x 17408)
+    over distinct layers in one CUDA graph, at --m token rows."""
+    import torch
+
+    from nvfp4_weight_only_gb300 import ffi, synth
+
+    H, I, M = 5120, 17408, args.m or 1
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    ffi.load(build_if_missing=True)
+    L = args.layers or 24
+    lyrs = build_w8a16_layers(ffi, synth, H, I, L, dev)
+    timer = GraphTimer(torch.cuda.Stream(device=dev))
+    peak, kind = measured_peaks()
+    entry, launches, _ = w8a16_case(ffi, synth, timer, dev, lyrs, H, I, M, args.act or 0,
+                                    args.steps, peak, kernels=True)
+    return {"metric": "µs per block-scaled FP8 FFN layer and effective HBM GB/s",
+            "value": entry["gbs"], "unit": "GB/s", **entry, "peak": peak, "peak_kind": kind,
+            "n_gpus": 1, "steps": args.steps, "warmup": 3, "higher_is_better": True,
+            "config": {"workload": f"FP8 (w8a16) SwiGLU FFN H={H} I={I} M={M}, {L} layers"},
+            "gpu_launches": launches}
+
+
 def cpu_baseline(wl, M, budget_s=10.0):
     """The oracle FFN on the host cores for one layer of the workload."""
     import numpy as np
@@ -670,11 +790,16 @@ def main():
     ap.add_argument("--sweep-reps", type=int, default=10)
     ap.add_argument("--gemv", default=None, metavar="N,K",
                     help="time the standalone GEMV of one N x K projection instead")
+    ap.add_argument("--w8a16", action="store_true",
+                    help="time the block-scaled FP8 FFN on the headline layer instead")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     wl = WORKLOADS[args.workload]
+    if args.w8a16:
+        print(json.dumps(run_w8a16(args)), flush=True)
+        return
     if args.gemv:
         print(json.dumps(run_gemv(args)), flush=True)
         return

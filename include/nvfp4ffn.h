@@ -291,6 +291,73 @@ nvfp4_status ffn_swiglu_nvfp4_noalloc(const void* x, int M, int H, int I,
  */
 nvfp4_status nvfp4_noalloc_status(cudaStream_t stream);
 
+/* ------------------------------------------------------ block-scaled FP8 (w8a16) */
+
+/*
+ * The dense-FFN page's native FP8 arm (DenseFfnWeightsFp8 and set_fp8_weights;
+ * the FP8 dispatch of DenseFfnLayer::forward: w8a16_gemv_dual for gate and up,
+ * then w8a16_gemv_silu_input for the down projection on the activation),
+ * weights used as loaded, with no NVFP4 requantisation.  A projection [N, K]:
+ *   codes (device) E4M3 bytes [N, K] row-major, the "fn" variant (0x7F/0xFF
+ *         are NaN, outside the contract);
+ *   grid  (device) fp32 [ceil(N/128), ceil(K/128)] row-major, 4-byte aligned;
+ *   W[n][k] = e4m3(codes[n][k]) * grid[n/128][k/128]  (the block grid the
+ *   weight loader's proj_is_fp8_any_scale accepts; a per-tensor scalar scale
+ *   is the uniform grid).
+ * The roundings are those of the NVFP4 path: g, u, h and out are bf16.  Every
+ * call below follows the conventions of its NVFP4 counterpart (status codes,
+ * validation before any launch, asynchronous on `stream`, the workspace
+ * contract, M up to 64 in groups of 16, K/H/I multiples of 16).
+ */
+
+/* Bytes of a repacked FP8 projection [N, K] / gate+up pair [I, H] (0 for
+ * invalid sizes): the codes, padded to 256 rows and 256 K, plus one fp32
+ * scale per 16 rows and 64 K. */
+size_t w8a16_repacked_bytes(int N, int K);
+size_t w8a16_repacked_gate_up_bytes(int I, int H);
+
+/* Canonical FP8 -> kernel layout (codes permuted, grid entries copied per
+ * 16-row tile and 64-K chunk; no arithmetic).  packed (device, out) >=
+ * w8a16_repacked_bytes(N, K), 16-byte aligned. */
+nvfp4_status w8a16_repack(const uint8_t* codes, const float* grid, int N, int K, void* packed,
+                          cudaStream_t stream);
+
+/* Gate and up [I, H] into one blob (each tile's gate and up codes back to
+ * back), >= w8a16_repacked_gate_up_bytes(I, H). */
+nvfp4_status w8a16_repack_gate_up(const uint8_t* gate_codes, const float* gate_grid,
+                                  const uint8_t* up_codes, const float* up_grid, int I, int H,
+                                  void* packed, cudaStream_t stream);
+
+/* Inverse of w8a16_repack (a test aid): codes [N, K] and grid. */
+nvfp4_status w8a16_unpack(const void* packed, int N, int K, uint8_t* codes, float* grid,
+                          cudaStream_t stream);
+
+/* Workspace bytes for w8a16_gemv; contract as for nvfp4_gemv. */
+size_t w8a16_gemv_workspace_bytes(int M, int N, int K);
+
+/*
+ * y[m][n] = bf16(sum_k x[m][k] * W[n][k]) for the FP8 projection (the page's
+ * w8a16_gemv):  x (device) bf16 [M, K];  packed_w from w8a16_repack(N, K);
+ * y (device, out) bf16 [M, N];  ws >= w8a16_gemv_workspace_bytes.
+ */
+nvfp4_status w8a16_gemv(const void* x, int M, int K, const void* packed_w, int N, void* y,
+                        void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Workspace bytes for ffn_swiglu_w8a16; h [M, I] lies at
+ * ffn_swiglu_nvfp4_hidden_offset() in it, as for ffn_swiglu_nvfp4. */
+size_t ffn_swiglu_w8a16_workspace_bytes(int M, int H, int I);
+
+/*
+ * The decode FFN on FP8 weights, in two launches:
+ *   1. g = bf16(gate.x), u = bf16(up.x), h = bf16(act(g) * u)   [M, I] in ws
+ *   2. out = bf16(down.h)                                        [M, H]
+ *   gate_up_packed from w8a16_repack_gate_up(I, H); down_packed from
+ *   w8a16_repack(H, I); other arguments as ffn_swiglu_nvfp4.
+ */
+nvfp4_status ffn_swiglu_w8a16(const void* x, int M, int H, int I, const void* gate_up_packed,
+                              const void* down_packed, nvfp4_act act, void* out, void* ws,
+                              size_t ws_bytes, cudaStream_t stream);
+
 /* ------------------------------------------------------------------ utilities */
 
 /* Zero-fill a workspace (asynchronous memset on `stream`). */

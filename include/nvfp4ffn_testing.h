@@ -32,6 +32,8 @@ nvfp4_status nvfp4_testing_inject_stall(int enable, unsigned long long wait_limi
  * launch is refused), -1 for invalid arguments.  Needs no GPU.
  */
 int nvfp4_testing_plan_aligned(int streams, int M, int N, int K, int num_sms);
+/* The same check for the block-scaled FP8 kernels (w8a16_gemv, ffn_swiglu_w8a16). */
+int nvfp4_testing_plan_aligned_w8a16(int streams, int M, int N, int K, int num_sms);
 
 #ifdef __cplusplus
 }

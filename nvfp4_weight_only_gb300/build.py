@@ -13,7 +13,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libnvfp4ffn.so")
-SOURCES = ["api.cu", "quantize.cu", "repack.cu", "stream_gemv.cu", "ffn_noalloc.cu", "lora.cu"]
+SOURCES = ["api.cu", "quantize.cu", "repack.cu", "stream_gemv.cu", "stream_gemv_fp8.cu",
+           "ffn_noalloc.cu", "lora.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", CSRC, "-I", os.path.join(ROOT, "include")]

@@ -45,18 +45,18 @@ int group_rows(int M, int g) {
 
 // Partial-sum bytes of the largest launch among M's groups (they run one
 // after another on the same stream, so they share one area).
-size_t group_partial_bytes(int streams, int M, int N, int K, int sms) {
-    size_t most = nvf::gemv_partial_bytes(streams, group_rows(M, 0), N, K, sms);
+size_t group_partial_bytes(int streams, int M, int N, int K, int sms, bool f8 = false) {
+    size_t most = nvf::gemv_partial_bytes(streams, group_rows(M, 0), N, K, sms, f8);
     const int last = group_rows(M, group_count(M) - 1);
-    const size_t b = nvf::gemv_partial_bytes(streams, last, N, K, sms);
+    const size_t b = nvf::gemv_partial_bytes(streams, last, N, K, sms, f8);
     return b > most ? b : most;
 }
 
 // GEMV workspace: [status][counter region][partials].  0 if N has more row
 // blocks than the counter region holds.
-size_t gemv_ws_bytes(int streams, int M, int N, int K, int sms) {
+size_t gemv_ws_bytes(int streams, int M, int N, int K, int sms, bool f8 = false) {
     if (nvf::gemv_counter_bytes(N) > nvf::kCounterRegionBytes) return 0;
-    return nvf::kDataOffset + round256(group_partial_bytes(streams, M, N, K, sms));
+    return nvf::kDataOffset + round256(group_partial_bytes(streams, M, N, K, sms, f8));
 }
 
 // FFN workspace: [status][counter region: dual's counters, then down's]
@@ -66,15 +66,15 @@ struct FfnLayout {
     bool fits;  // both kernels' counters fit the counter region
 };
 
-FfnLayout ffn_layout(int M, int H, int I, int sms) {
+FfnLayout ffn_layout(int M, int H, int I, int sms, bool f8 = false) {
     FfnLayout l;
     l.down_cnt_off = nvf::gemv_counter_bytes(I);
     l.fits = l.down_cnt_off + nvf::gemv_counter_bytes(H) <= nvf::kCounterRegionBytes;
     l.h_off = nvf::kDataOffset;
     l.dual_off = l.h_off + round256((size_t)M * I * 2);
-    l.dual_bytes = round256(group_partial_bytes(2, M, I, H, sms));
+    l.dual_bytes = round256(group_partial_bytes(2, M, I, H, sms, f8));
     l.down_off = l.dual_off + l.dual_bytes;
-    l.down_bytes = round256(group_partial_bytes(1, M, H, I, sms));
+    l.down_bytes = round256(group_partial_bytes(1, M, H, I, sms, f8));
     l.total = l.down_off + l.down_bytes;
     return l;
 }
@@ -422,6 +422,126 @@ int nvfp4_testing_plan_aligned(int streams, int M, int N, int K, int num_sms) {
     if ((streams != 1 && streams != 2) || M < 1 || M > 16 || N < 1 || K < 16 || num_sms < 1)
         return -1;
     return nvf::gemv_plan_aligned(streams, M, N, K, num_sms) ? 1 : 0;
+}
+
+int nvfp4_testing_plan_aligned_w8a16(int streams, int M, int N, int K, int num_sms) {
+    if ((streams != 1 && streams != 2) || M < 1 || M > 16 || N < 1 || K < 16 || num_sms < 1)
+        return -1;
+    return nvf::gemv_plan_aligned(streams, M, N, K, num_sms, true) ? 1 : 0;
+}
+
+/* ------------------------------------------------------------ block-scaled FP8 */
+
+size_t w8a16_repacked_bytes(int N, int K) {
+    if (N < 1 || K < 16) return 0;
+    return nvf::repacked_bytes_f8(N, K, 1);
+}
+
+size_t w8a16_repacked_gate_up_bytes(int I, int H) {
+    if (I < 1 || H < 16) return 0;
+    return nvf::repacked_bytes_f8(I, H, 2);
+}
+
+static bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+nvfp4_status w8a16_repack(const uint8_t* codes, const float* grid, int N, int K, void* packed,
+                          cudaStream_t stream) {
+    if (!codes || !grid || !packed) return NVFP4_ERR_NULL;
+    if (N < 1 || K < 16 || K % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (!aligned16(packed) || !aligned4(grid)) return NVFP4_ERR_ALIGN;
+    return cuda_status(nvf::launch_repack_f8(codes, grid, N, K,
+                                             reinterpret_cast<uint8_t*>(packed), 1, 0, stream));
+}
+
+nvfp4_status w8a16_repack_gate_up(const uint8_t* gate_codes, const float* gate_grid,
+                                  const uint8_t* up_codes, const float* up_grid, int I, int H,
+                                  void* packed, cudaStream_t stream) {
+    if (!gate_codes || !gate_grid || !up_codes || !up_grid || !packed) return NVFP4_ERR_NULL;
+    if (I < 1 || H < 16 || H % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (!aligned16(packed) || !aligned4(gate_grid) || !aligned4(up_grid)) return NVFP4_ERR_ALIGN;
+    uint8_t* p = reinterpret_cast<uint8_t*>(packed);
+    cudaError_t e = nvf::launch_repack_f8(gate_codes, gate_grid, I, H, p, 2, 0, stream);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    return cuda_status(nvf::launch_repack_f8(up_codes, up_grid, I, H, p, 2, 1, stream));
+}
+
+nvfp4_status w8a16_unpack(const void* packed, int N, int K, uint8_t* codes, float* grid,
+                          cudaStream_t stream) {
+    if (!packed || !codes || !grid) return NVFP4_ERR_NULL;
+    if (N < 1 || K < 16 || K % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (!aligned16(packed) || !aligned4(grid)) return NVFP4_ERR_ALIGN;
+    return cuda_status(nvf::launch_unpack_f8(reinterpret_cast<const uint8_t*>(packed), N, K,
+                                             codes, grid, stream));
+}
+
+size_t w8a16_gemv_workspace_bytes(int M, int N, int K) {
+    if (M < 1 || M > kMaxTokens || N < 1 || K < 16) return 0;
+    return gemv_ws_bytes(1, M, N, K, sms_for_sizing(), true);
+}
+
+nvfp4_status w8a16_gemv(const void* x, int M, int K, const void* packed_w, int N, void* y,
+                        void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!x || !packed_w || !y || !ws) return NVFP4_ERR_NULL;
+    if (M < 1 || M > kMaxTokens) return NVFP4_ERR_RANGE;
+    if (N < 1 || K < 16 || K % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(packed_w) || !aligned16(y) || !aligned16(ws))
+        return NVFP4_ERR_ALIGN;
+    if (overlap(x, (size_t)M * K * 2, y, (size_t)M * N * 2)) return NVFP4_ERR_ALIAS;
+    const int sms = nvf::device_sm_count();
+    if (sms <= 0) return NVFP4_ERR_CUDA;
+    const size_t need = gemv_ws_bytes(1, M, N, K, sms, true);
+    if (need == 0) return NVFP4_ERR_SHAPE;
+    if (ws_bytes < need) return NVFP4_ERR_WORKSPACE;
+    char* w = reinterpret_cast<char*>(ws);
+    for (int g = 0; g < group_count(M); ++g) {
+        const size_t r0 = (size_t)g * kGroupTokens;
+        const cudaError_t e = nvf::launch_stream_gemv_f8(
+            1, reinterpret_cast<const char*>(x) + r0 * K * 2, group_rows(M, g), K, packed_w, N, 0,
+            reinterpret_cast<char*>(y) + r0 * N * 2, reinterpret_cast<int*>(w),
+            reinterpret_cast<int*>(w + nvf::kStatusBytes), w + nvf::kDataOffset,
+            need - nvf::kDataOffset, sms, true, stream);
+        if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    }
+    return NVFP4_OK;
+}
+
+size_t ffn_swiglu_w8a16_workspace_bytes(int M, int H, int I) {
+    if (M < 1 || M > kMaxTokens || H < 16 || I < 16) return 0;
+    const FfnLayout l = ffn_layout(M, H, I, sms_for_sizing(), true);
+    return l.fits ? l.total : 0;
+}
+
+nvfp4_status ffn_swiglu_w8a16(const void* x, int M, int H, int I, const void* gate_up_packed,
+                              const void* down_packed, nvfp4_act act, void* out, void* ws,
+                              size_t ws_bytes, cudaStream_t stream) {
+    if (!ws) return NVFP4_ERR_NULL;
+    const int v = nvf::validate_ffn_args(x, M, H, I, gate_up_packed, down_packed, (int)act, out);
+    if (v != NVFP4_OK) return (nvfp4_status)v;
+    if (!aligned16(ws)) return NVFP4_ERR_ALIGN;
+    const int sms = nvf::device_sm_count();
+    if (sms <= 0) return NVFP4_ERR_CUDA;
+    const FfnLayout l = ffn_layout(M, H, I, sms, true);
+    if (!l.fits) return NVFP4_ERR_SHAPE;
+    if (ws_bytes < l.total) return NVFP4_ERR_WORKSPACE;
+    char* w = reinterpret_cast<char*>(ws);
+    int* status = reinterpret_cast<int*>(w);
+    int* counters = reinterpret_cast<int*>(w + nvf::kStatusBytes);
+    char* h = w + l.h_off;
+    for (int g = 0; g < group_count(M); ++g) {
+        const size_t r0 = (size_t)g * kGroupTokens;
+        const int mg = group_rows(M, g);
+        char* hg = h + r0 * I * 2;
+        cudaError_t e = nvf::launch_stream_gemv_f8(
+            2, reinterpret_cast<const char*>(x) + r0 * H * 2, mg, H, gate_up_packed, I, (int)act,
+            hg, status, counters, w + l.dual_off, l.dual_bytes, sms, true, stream);
+        if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+        e = nvf::launch_stream_gemv_f8(1, hg, mg, I, down_packed, H, 0,
+                                       reinterpret_cast<char*>(out) + r0 * H * 2, status,
+                                       counters + l.down_cnt_off / sizeof(int), w + l.down_off,
+                                       l.down_bytes, sms, true, stream);
+        if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    }
+    return NVFP4_OK;
 }
 
 const char* nvfp4_status_string(nvfp4_status status) {

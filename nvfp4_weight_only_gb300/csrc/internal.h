@@ -15,6 +15,12 @@ cudaError_t launch_repack(const uint8_t* codes, const uint8_t* scales, int N, in
                           uint8_t* packed, int streams, int stream_index, cudaStream_t s);
 cudaError_t launch_unpack(const uint8_t* packed, int N, int K, uint8_t* codes, uint8_t* scales,
                           cudaStream_t s);
+// Block-scaled FP8: E4M3 bytes [N, K] + FP32 grid [ceil(N/128), ceil(K/128)]
+// <-> the FP8 fragment layout (layout.h); stream_index of `streams`.
+cudaError_t launch_repack_f8(const uint8_t* codes, const float* grid, int N, int K,
+                             uint8_t* packed, int streams, int stream_index, cudaStream_t s);
+cudaError_t launch_unpack_f8(const uint8_t* packed, int N, int K, uint8_t* codes, float* grid,
+                             cudaStream_t s);
 
 // stream_gemv.cu
 // Every GEMV/FFN workspace starts with a status word area, then one fixed
@@ -26,8 +32,9 @@ constexpr size_t kStatusBytes = 256;
 constexpr size_t kCounterRegionBytes = 128u << 10;
 constexpr size_t kDataOffset = kStatusBytes + kCounterRegionBytes;
 
-// fp32 partial-sum bytes of one launch, and the counter bytes for N rows.
-size_t gemv_partial_bytes(int streams, int M, int N, int K, int num_sms);
+// fp32 partial-sum bytes of one launch (f8: block-scaled FP8 weights), and
+// the counter bytes for N rows.
+size_t gemv_partial_bytes(int streams, int M, int N, int K, int num_sms, bool f8 = false);
 size_t gemv_counter_bytes(int N);
 // lora_deltas (streams == 2, may be null): bf16 [M, N] deltas added to the
 // rounded gate and up values before the activation, g = bf16(g + delta_g);
@@ -39,6 +46,17 @@ cudaError_t launch_stream_gemv(int streams, const void* x, int M, int K, const v
                                const void* const* lora_deltas = nullptr);
 
 int device_sm_count();
+
+// stream_gemv_fp8.cu: the same kernels on block-scaled FP8 weights (repacked
+// by launch_repack_f8); no per-tensor scale, no adapter deltas.
+cudaError_t launch_stream_gemv_f8(int streams, const void* x, int M, int K, const void* packed,
+                                  int N, int act, void* out, int* status, int* counters,
+                                  void* partials, size_t partial_bytes, int num_sms,
+                                  bool early_weights, cudaStream_t s);
+
+// The testing switch's current values (set_test_stall).
+unsigned long long test_wait_ns();
+int test_stall();
 
 // lora.cu: the adapter overlay, dW = B A (A [r, K], B [N, r], bf16).
 constexpr int kLoraMaxRank = 64;
@@ -60,7 +78,7 @@ cudaError_t launch_lora_delta(const void* const* part, int K, const void* const*
 
 // Whether the kernel's shared-memory plan for this problem has the alignment
 // its accesses assume (the launcher refuses plans that do not).
-bool gemv_plan_aligned(int streams, int M, int N, int K, int num_sms);
+bool gemv_plan_aligned(int streams, int M, int N, int K, int num_sms, bool f8 = false);
 
 // Testing only: with stall != 0 every later GEMV/FFN launch runs with a
 // producer that issues no copies and bounded waits of wait_ns, so each

@@ -59,4 +59,32 @@ inline size_t repacked_bytes(int N, int K, int streams) {
     return (size_t)g.RB * g.C * kBlockTiles * kUnitBytes * streams;
 }
 
+// ---- block-scaled FP8 (the dense-FFN page's DenseFfnWeightsFp8: E4M3 bytes
+// [N, K] row-major and an FP32 grid [ceil(N/128), ceil(K/128)], weight =
+// e4m3(q[n][k]) * grid[n/128][k/128]) in the same row blocks and chunks:
+//
+//   tile   = 16 rows x 64 K = 1024 code bytes; lane L = 4g + t owns bytes
+//            [32L, 32L+32), byte 8j + 2r + e (j = k16 block 0..3, r = 0..3,
+//            e = 0, 1) holding the canonical byte of row g + 8*(r&1) at
+//            K = 16j + 2t + 8*(r>>1) + e: registers a0..a3 of block j, two
+//            E4M3 per f16x2 register;
+//   group  = one (row block, chunk): the 16 tiles' codes (tile-major, the
+//            streams of a tile back to back), then one fp32 per tile and
+//            stream: the grid entry of the tile's 128-row block at the
+//            chunk's 128-K block (every 16-row tile lies inside one 128-row
+//            block, and every 64-K chunk inside one 128-K block);
+//   order  = [row block][chunk], like the NVFP4 layout.
+// Padding rows and K carry zero codes and a zero scale.
+constexpr int kF8TileBytes = 1024;
+
+inline size_t f8_group_bytes_host(int streams) {
+    return (size_t)streams * (kBlockTiles * kF8TileBytes + kBlockTiles * 4);
+}
+
+// Bytes of one repacked FP8 projection (streams = 1) or gate/up pair (2).
+inline size_t repacked_bytes_f8(int N, int K, int streams) {
+    Geometry g = geometry(N, K);
+    return (size_t)g.RB * g.C * f8_group_bytes_host(streams);
+}
+
 }  // namespace nvf

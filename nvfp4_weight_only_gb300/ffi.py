@@ -35,10 +35,14 @@ EXPORTS = [
     "ffn_swiglu_nvfp4_noalloc", "nvfp4_noalloc_status",
     "ffn_swiglu_nvfp4_lora_workspace_bytes", "ffn_swiglu_nvfp4_lora",
     "nvfp4_lora_apply_scratch_bytes", "nvfp4_lora_apply",
+    "w8a16_repacked_bytes", "w8a16_repacked_gate_up_bytes", "w8a16_repack",
+    "w8a16_repack_gate_up", "w8a16_unpack", "w8a16_gemv_workspace_bytes", "w8a16_gemv",
+    "ffn_swiglu_w8a16_workspace_bytes", "ffn_swiglu_w8a16",
     "nvfp4_workspace_init", "nvfp4_workspace_status", "nvfp4_status_string",
 ]
 # Every symbol declared in include/nvfp4ffn_testing.h (test hooks).
-TESTING_EXPORTS = ["nvfp4_testing_inject_stall", "nvfp4_testing_plan_aligned"]
+TESTING_EXPORTS = ["nvfp4_testing_inject_stall", "nvfp4_testing_plan_aligned",
+                   "nvfp4_testing_plan_aligned_w8a16"]
 
 
 class Nvfp4Error(RuntimeError):
@@ -88,6 +92,16 @@ def load(build_if_missing: bool = False):
         "nvfp4_lora_apply": (i32, [vp, i32, i32, vp, vp, i32, i32, vp, vp, sz, vp]),
         "nvfp4_testing_inject_stall": (i32, [i32, ctypes.c_ulonglong]),
         "nvfp4_testing_plan_aligned": (i32, [i32, i32, i32, i32, i32]),
+        "nvfp4_testing_plan_aligned_w8a16": (i32, [i32, i32, i32, i32, i32]),
+        "w8a16_repacked_bytes": (sz, [i32, i32]),
+        "w8a16_repacked_gate_up_bytes": (sz, [i32, i32]),
+        "w8a16_repack": (i32, [vp, vp, i32, i32, vp, vp]),
+        "w8a16_repack_gate_up": (i32, [vp, vp, vp, vp, i32, i32, vp, vp]),
+        "w8a16_unpack": (i32, [vp, i32, i32, vp, vp, vp]),
+        "w8a16_gemv_workspace_bytes": (sz, [i32, i32, i32]),
+        "w8a16_gemv": (i32, [vp, i32, i32, vp, i32, vp, vp, sz, vp]),
+        "ffn_swiglu_w8a16_workspace_bytes": (sz, [i32, i32, i32]),
+        "ffn_swiglu_w8a16": (i32, [vp, i32, i32, i32, vp, vp, i32, vp, vp, sz, vp]),
         "nvfp4_workspace_init": (i32, [vp, sz, vp]),
         "nvfp4_workspace_status": (i32, [vp, vp]),
         "nvfp4_status_string": (ctypes.c_char_p, [i32]),
@@ -342,3 +356,85 @@ def nvfp4_noalloc_status(device=None) -> int:
     """Status of the fixed-workspace FFN calls (0 = OK, 7 = timeout, after which
     the library has zero-filled its array again)."""
     return load().nvfp4_noalloc_status(_stream(device))
+
+
+# ------------------------------------------------------------------ block-scaled FP8 (w8a16)
+
+def _fp8_projection(codes, grid, name):
+    _cuda(codes, f"{name} codes", torch.uint8)
+    _cuda(grid, f"{name} grid", torch.float32)
+    N, K = codes.shape
+    if tuple(grid.shape) != ((N + 127) // 128, (K + 127) // 128):
+        raise ValueError(f"{name} grid must be [ceil(N/128), ceil(K/128)], got {tuple(grid.shape)}")
+    return N, K
+
+
+def w8a16_repack(codes: torch.Tensor, grid: torch.Tensor) -> torch.Tensor:
+    """E4M3 bytes [N, K] + fp32 block grid -> the kernel layout (uint8 blob)."""
+    N, K = _fp8_projection(codes, grid, "w8a16_repack")
+    L = load()
+    out = torch.empty(L.w8a16_repacked_bytes(N, K), dtype=torch.uint8, device=codes.device)
+    _check("w8a16_repack", L.w8a16_repack(_ptr(codes), _ptr(grid), N, K, _ptr(out),
+                                          _stream(codes.device)))
+    return out
+
+
+def w8a16_repack_gate_up(gate_codes, gate_grid, up_codes, up_grid) -> torch.Tensor:
+    I, H = _fp8_projection(gate_codes, gate_grid, "gate")
+    if _fp8_projection(up_codes, up_grid, "up") != (I, H):
+        raise ValueError("gate and up must have the same shape")
+    L = load()
+    out = torch.empty(L.w8a16_repacked_gate_up_bytes(I, H), dtype=torch.uint8,
+                      device=gate_codes.device)
+    _check("w8a16_repack_gate_up",
+           L.w8a16_repack_gate_up(_ptr(gate_codes), _ptr(gate_grid), _ptr(up_codes),
+                                  _ptr(up_grid), I, H, _ptr(out), _stream(gate_codes.device)))
+    return out
+
+
+def w8a16_unpack(packed: torch.Tensor, N: int, K: int):
+    _cuda(packed, "packed", torch.uint8)
+    L = load()
+    codes = torch.empty((N, K), dtype=torch.uint8, device=packed.device)
+    grid = torch.empty(((N + 127) // 128, (K + 127) // 128), dtype=torch.float32,
+                       device=packed.device)
+    _check("w8a16_unpack", L.w8a16_unpack(_ptr(packed), N, K, _ptr(codes), _ptr(grid),
+                                          _stream(packed.device)))
+    return codes, grid
+
+
+def w8a16_gemv(x: torch.Tensor, packed_w: torch.Tensor, N: int, ws: torch.Tensor = None,
+               out: torch.Tensor = None) -> torch.Tensor:
+    """y bf16 [M, N] = one block-scaled FP8 projection of x bf16 [M, K]."""
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(packed_w, "packed_w", torch.uint8)
+    M, K = x.shape
+    L = load()
+    if ws is None:
+        ws = workspace(L.w8a16_gemv_workspace_bytes(M, N, K), x.device)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _cuda(out, "out", torch.bfloat16)
+    _check("w8a16_gemv", L.w8a16_gemv(_ptr(x), M, K, _ptr(packed_w), N, _ptr(out), _ptr(ws),
+                                      ws.numel(), _stream(x.device)))
+    return out
+
+
+def ffn_swiglu_w8a16(x: torch.Tensor, gate_up_packed: torch.Tensor, down_packed: torch.Tensor,
+                     I: int, act: int = NVFP4_ACT_SILU, ws: torch.Tensor = None,
+                     out: torch.Tensor = None) -> torch.Tensor:
+    """out bf16 [M, H] = down(act(gate(x)) * up(x)) on block-scaled FP8 weights."""
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(gate_up_packed, "gate_up_packed", torch.uint8)
+    _cuda(down_packed, "down_packed", torch.uint8)
+    M, H = x.shape
+    L = load()
+    if ws is None:
+        ws = workspace(L.ffn_swiglu_w8a16_workspace_bytes(M, H, I), x.device)
+    if out is None:
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    _cuda(out, "out", torch.bfloat16)
+    _check("ffn_swiglu_w8a16",
+           L.ffn_swiglu_w8a16(_ptr(x), M, H, I, _ptr(gate_up_packed), _ptr(down_packed), int(act),
+                              _ptr(out), _ptr(ws), ws.numel(), _stream(x.device)))
+    return out

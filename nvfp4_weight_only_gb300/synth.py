@@ -10,7 +10,12 @@ checkpoints replaced by draws of the same shapes):
     positions multiplied by 20 (the outlier variant of the batch-M workload);
   * weights fp32 ~ N(0, 0.02), later quantised to NVFP4 by the library;
   * seeds: x uses seed 0 unless told otherwise; layer l uses 1000 + l with the
-    gate / up / down projections as sub-streams 0 / 1 / 2.
+    gate / up / down projections as sub-streams 0 / 1 / 2;
+  * block-scaled FP8 projections (stand-ins for an FP8 checkpoint, which the
+    pages load as they are): E4M3 bytes of N(0, 1) * 448/4.5 draws (torch's
+    float8_e4m3fn conversion, saturated at +-448) and an fp32 block grid of
+    std * 4.5/448 * U(0.75, 1.25), one draw per 128 x 128 block, so the weights
+    spread like N(0, std^2) and every block has its own scale.
 """
 import torch
 
@@ -32,6 +37,16 @@ def weights_f32(N: int, K: int, seed: int, std: float = 0.02, device="cpu") -> t
     """fp32 [N, K] ~ N(0, std^2)."""
     g = _gen(seed, device)
     return torch.randn((N, K), generator=g, dtype=torch.float32, device=device) * std
+
+
+def fp8_weights(N: int, K: int, seed: int, std: float = 0.02, device="cpu"):
+    """(E4M3 bytes uint8 [N, K], fp32 grid [ceil(N/128), ceil(K/128)]) as above."""
+    g = _gen(seed, device)
+    v = torch.randn((N, K), generator=g, dtype=torch.float32, device=device) * (448.0 / 4.5)
+    codes = v.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    shape = ((N + 127) // 128, (K + 127) // 128)
+    u = torch.rand(shape, generator=g, dtype=torch.float32, device=device)
+    return codes, (std * 4.5 / 448.0) * (0.75 + 0.5 * u)
 
 
 def activations_bf16(M: int, K: int, seed: int = 0, outlier_frac: float = 0.0,

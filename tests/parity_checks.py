@@ -155,3 +155,31 @@ def lora_delta_interval(v_lo, v_hi, A_bits, B_bits, acc_eps=ACC_EPS):
 def check_interval(got_bits, lo, hi, ref_bits, what):
     """got inside [lo, hi] everywhere, equal to ref wherever lo == hi."""
     return _stats(bf16_f64(got_bits), lo, hi, bf16_f64(ref_bits), what)
+
+
+# ------------------------------------------------------------ block-scaled FP8
+
+def abs_sum_fp8(x_bits, q):
+    """sum_k |x_k| |W[n][k]| for an FP8 projection q = (codes, grid)."""
+    return oracle.gemv_fp8_f64((np.asarray(x_bits, np.uint16) & 0x7FFF).astype(np.uint16),
+                               (np.asarray(q[0], np.uint8) & 0x7F).astype(np.uint8),
+                               np.abs(np.asarray(q[1], np.float32)))
+
+
+def gemv_interval_fp8(x_bits, q, acc_eps=ACC_EPS):
+    v = oracle.gemv_fp8_f64(x_bits, q[0], q[1])
+    return rounding_interval(v, acc_eps * abs_sum_fp8(x_bits, q))
+
+
+def check_gemv_fp8(y_bits, x_bits, q, what="w8a16 gemv", acc_eps=ACC_EPS):
+    lo, hi = gemv_interval_fp8(x_bits, q, acc_eps)
+    ref = oracle.bf16_bits_to_f64(oracle.gemv_fp8(x_bits, q[0], q[1]))
+    return _stats(oracle.bf16_bits_to_f64(y_bits), lo, hi, ref, what)
+
+
+def check_hidden_fp8(h_bits, x_bits, gate, up, act, what="w8a16 h", acc_eps=ACC_EPS):
+    g_lo, g_hi = gemv_interval_fp8(x_bits, gate, acc_eps)
+    u_lo, u_hi = gemv_interval_fp8(x_bits, up, acc_eps)
+    lo, hi = hidden_interval_from(g_lo, g_hi, u_lo, u_hi, act)
+    ref = oracle.bf16_bits_to_f64(oracle.ffn_fp8_hidden(x_bits, gate, up, act))
+    return _stats(oracle.bf16_bits_to_f64(h_bits), lo, hi, ref, what)

@@ -156,3 +156,44 @@ def test_noalloc_validation_touches_nothing(lib):
     assert f(A[0], 1, 256, 512, A[1], 1.0, 1.0, A[2], 1.0, 0, A[0], S) == 8
     B = [ctypes.c_void_p(0x10000000 * i) for i in range(1, 5)]  # disjoint at this size
     assert f(B[0], 16, 8192, 32768, B[1], 1.0, 1.0, B[2], 1.0, 0, B[3], S) == 5
+
+
+def test_w8a16_repacked_sizes(lib):
+    """FP8 blobs: the codes (N*K bytes for shapes that are multiples of 256)
+    plus one fp32 scale per 16-row tile and 64-K chunk (1/256 more)."""
+    for N, K in ((5120, 17408), (17408, 5120), (4096, 4096), (256, 256)):
+        assert lib.w8a16_repacked_bytes(N, K) == N * K + N * K // 256
+        assert lib.w8a16_repacked_gate_up_bytes(N, K) == 2 * (N * K + N * K // 256)
+    assert lib.w8a16_repacked_bytes(200, 272) == 256 * 512 * (1 + 1 / 256)
+    assert lib.w8a16_repacked_bytes(0, 64) == 0
+
+
+def test_w8a16_plans_are_aligned(lib):
+    shapes = [(5120, 17408), (17408, 5120), (4096, 12288), (12288, 4096), (65536, 21504),
+              (4096, 4096), (200, 272), (16, 16), (1, 2048), (300, 21504)]
+    for streams in (1, 2):
+        for M in range(1, 17):
+            for N, K in shapes:
+                for sms in (152, 148, 7, 1):
+                    assert lib.nvfp4_testing_plan_aligned_w8a16(streams, M, N, K, sms) == 1, \
+                        (streams, M, N, K, sms)
+
+
+def test_w8a16_validation_before_any_launch(lib):
+    """Argument errors of the FP8 calls come back without a GPU."""
+    p = ctypes.c_void_p(0x10000000)
+    q = ctypes.c_void_p(0x20000000)
+    ws = ctypes.c_void_p(0x30000000)
+    f = lib.ffn_swiglu_w8a16
+    assert f(None, 1, 256, 512, p, q, 0, ws, ws, 1 << 20, None) == 1           # null x
+    assert f(p, 0, 256, 512, p, q, 0, q, ws, 1 << 20, None) == 4              # M = 0
+    assert f(p, 65, 256, 512, p, q, 0, q, ws, 1 << 20, None) == 4             # M = 65
+    assert f(p, 1, 250, 512, p, q, 0, q, ws, 1 << 20, None) == 2              # H % 16
+    assert f(p, 1, 256, 512, p, q, 7, q, ws, 1 << 20, None) == 4              # act
+    assert f(ctypes.c_void_p(0x10000004), 1, 256, 512, p, q, 0, q, ws, 1 << 20, None) == 3
+    g = lib.w8a16_gemv
+    assert g(p, 1, 250, q, 64, ws, ws, 1 << 20, None) == 2                    # K % 16
+    assert g(p, 1, 256, q, 64, p, ws, 1 << 20, None) == 8                     # x and y overlap
+    r = lib.w8a16_repack
+    assert r(p, ctypes.c_void_p(0x20000002), 256, 256, q, None) == 3         # grid alignment
+    assert r(p, q, 256, 8, q, None) == 2
