@@ -119,6 +119,30 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
     return old;
 }
 
+// Load with acquire semantics at GPU scope.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Polls *p (acquire) until it reaches `target`.  Gives up (returns false)
+// after limit_ns, or when *abort is set by another warp.
+__device__ __forceinline__ bool wait_count_bounded(const int* p, int target,
+                                                   const volatile int* abort,
+                                                   unsigned long long limit_ns) {
+    if (ld_acquire_gpu(p) >= target) return true;
+    const unsigned long long t0 = global_timer_ns();
+    unsigned pause = 32;  // ns, doubled up to 512 to keep the polling light
+    for (;;) {
+        __nanosleep(pause);
+        if (pause < 512) pause *= 2;
+        if (ld_acquire_gpu(p) >= target) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }

@@ -60,19 +60,26 @@ cudaError_t launch_stream_gemv(int streams, const void* x, int M, int K, const v
                          partials, early_weights);
     a.lora_dg = lora_deltas ? reinterpret_cast<const __nv_bfloat16*>(lora_deltas[0]) : nullptr;
     a.lora_du = lora_deltas ? reinterpret_cast<const __nv_bfloat16*>(lora_deltas[1]) : nullptr;
-    const bool em = p.part_stride != 0;
+    // one token tile (M <= 8) always takes element-major partials
+    static_assert(kElemMajorMaxM == 8, "element-major partials exactly when NT == 1");
+    if ((p.part_stride != 0) != (p.NT == 1)) return cudaErrorInvalidValue;
+    const bool coop = use_coop(p, M);
     if (streams == 1) {
-        if (M == 1) return launch_t<1, 1, true, true, true, false>(p, a, s);
-        if (M == 2) return launch_t<1, 1, false, true, true, false>(p, a, s);
-        if (em) return launch_t<1, 1, false, false, true, false>(p, a, s);
-        return p.NT == 1 ? launch_t<1, 1, false, false, false, false>(p, a, s)
-                         : launch_t<1, 2, false, false, false, false>(p, a, s);
+        if (M == 1) return launch_t<1, 1, true, true, true, false, false>(p, a, s);
+        if (M == 2) return launch_t<1, 1, false, true, true, false, false>(p, a, s);
+        if (p.NT == 1)
+            return coop ? launch_t<1, 1, false, false, true, false, true>(p, a, s)
+                        : launch_t<1, 1, false, false, true, false, false>(p, a, s);
+        return coop ? launch_t<1, 2, false, false, false, false, true>(p, a, s)
+                    : launch_t<1, 2, false, false, false, false, false>(p, a, s);
     }
-    if (M == 1) return launch_t<2, 1, true, true, true, false>(p, a, s);
-    if (M == 2) return launch_t<2, 1, false, true, true, false>(p, a, s);
-    if (em) return launch_t<2, 1, false, false, true, false>(p, a, s);
-    return p.NT == 1 ? launch_t<2, 1, false, false, false, false>(p, a, s)
-                     : launch_t<2, 2, false, false, false, false>(p, a, s);
+    if (M == 1) return launch_t<2, 1, true, true, true, false, false>(p, a, s);
+    if (M == 2) return launch_t<2, 1, false, true, true, false, false>(p, a, s);
+    if (p.NT == 1)
+        return coop ? launch_t<2, 1, false, false, true, false, true>(p, a, s)
+                    : launch_t<2, 1, false, false, true, false, false>(p, a, s);
+    return coop ? launch_t<2, 2, false, false, false, false, true>(p, a, s)
+                : launch_t<2, 2, false, false, false, false, false>(p, a, s);
 }
 
 }  // namespace nvf

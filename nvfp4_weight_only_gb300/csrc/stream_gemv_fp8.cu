@@ -19,14 +19,21 @@ cudaError_t launch_stream_gemv_f8(int streams, const void* x, int M, int K, cons
     // one token tile (M <= 8) always takes element-major partials
     static_assert(kElemMajorMaxM == 8, "element-major partials exactly when NT == 1");
     if ((p.part_stride != 0) != (p.NT == 1)) return cudaErrorInvalidValue;
+    const bool coop = use_coop(p, M);
     if (streams == 1) {
-        if (M == 1) return launch_t<1, 1, true, false, true, true>(p, a, s);
-        if (p.NT == 1) return launch_t<1, 1, false, false, true, true>(p, a, s);
-        return launch_t<1, 2, false, false, false, true>(p, a, s);
+        if (M == 1) return launch_t<1, 1, true, false, true, true, false>(p, a, s);
+        if (p.NT == 1)
+            return coop ? launch_t<1, 1, false, false, true, true, true>(p, a, s)
+                        : launch_t<1, 1, false, false, true, true, false>(p, a, s);
+        return coop ? launch_t<1, 2, false, false, false, true, true>(p, a, s)
+                    : launch_t<1, 2, false, false, false, true, false>(p, a, s);
     }
-    if (M == 1) return launch_t<2, 1, true, false, true, true>(p, a, s);
-    if (p.NT == 1) return launch_t<2, 1, false, false, true, true>(p, a, s);
-    return launch_t<2, 2, false, false, false, true>(p, a, s);
+    if (M == 1) return launch_t<2, 1, true, false, true, true, false>(p, a, s);
+    if (p.NT == 1)
+        return coop ? launch_t<2, 1, false, false, true, true, true>(p, a, s)
+                    : launch_t<2, 1, false, false, true, true, false>(p, a, s);
+    return coop ? launch_t<2, 2, false, false, false, true, true>(p, a, s)
+                : launch_t<2, 2, false, false, false, true, false>(p, a, s);
 }
 
 }  // namespace nvf

@@ -574,13 +574,18 @@ __device__ __forceinline__ bool resolve_tile(const KArgs& a, int rb, int warp, i
 // CTA's first kMaxEvents such segments (event evt) by the publisher warp,
 // asynchronously (returns -2 - evt), later ones by this warp (returns the
 // counter's old value, lane 0).  Whether this range arrived last, and so must
-// reduce the tile, is resolved after the stream (resolve_pending).
+// reduce the tile, is resolved after the stream (resolve_pending).  With
+// coop_last (a range's last segment in the cooperative kernels) the partial is
+// stored and kSegCoop returned: the caller then finishes the tile with
+// coop_finish.  (Publisher events return -2 .. -1 - kMaxEvents.)
+constexpr int kSegCoop = -1000;
+static_assert(kSegCoop < -1 - kMaxEvents, "kSegCoop must not be a publisher event code");
 template <int NS, int NT, bool DIAG, bool EM>
 __device__ __forceinline__ int finish_segment(const KArgs& a, float (&hi)[NS][NT][4],
                                                float (&lo)[NS][NT][4],
                                                const float (&unscale)[NT][2], int r, int q0,
                                                int rb, int cb_last, int warp, int lane, bool ok,
-                                               int evt, uint32_t seg_done0) {
+                                               int evt, uint32_t seg_done0, bool coop_last) {
     const int g = lane >> 2, tq = lane & 3;
     const int seg_lo = q0 > rb * a.CS ? q0 : rb * a.CS;
     const bool full_cover = (seg_lo == rb * a.CS) && (cb_last == a.CS - 1);
@@ -643,6 +648,7 @@ __device__ __forceinline__ int finish_segment(const KArgs& a, float (&hi)[NS][NT
                 }
     }
     __syncwarp();
+    if (coop_last) return kSegCoop;
     if (evt < kMaxEvents) {
         // the publisher warp counts the tile in once every warp has stored;
         // this warp streams on (the arrive releases the lanes' slot stores to
@@ -659,7 +665,8 @@ __device__ __forceinline__ int finish_segment(const KArgs& a, float (&hi)[NS][NT
 // kB ranges are issued before any is used, so a tile costs one load latency
 // per kB ranges whatever M is.
 template <int NS, int NT>
-__device__ __forceinline__ void reduce_tile(const KArgs& a, int rb, int warp, int lane, bool ok) {
+__device__ __forceinline__ void reduce_tile(const KArgs& a, int rb, int warp, int lane, bool ok,
+                                            int e_begin, int e_end) {
     constexpr int kIter = kTileRows * 8 * NT / 32;  // elements per lane at M = 8 NT
     constexpr int kB = 32 / (kIter * NS);           // ranges per batch (32 loads in flight)
     const long long p_lo = (long long)rb * a.CS;
@@ -678,10 +685,10 @@ __device__ __forceinline__ void reduce_tile(const KArgs& a, int rb, int warp, in
             const float* sl = rr <= r_last ? tile_slot<NS>(a, rr, rb, warp) : nullptr;
 #pragma unroll
             for (int i = 0; i < kIter; ++i) {
-                const int e = lane + 32 * i;
+                const int e = e_begin + lane + 32 * i;
 #pragma unroll
                 for (int si = 0; si < NS; ++si)
-                    part[b][i][si] = (sl != nullptr && e < n_el) ? __ldcg(sl + si * n_el + e) : 0.0f;
+                    part[b][i][si] = (sl != nullptr && e < e_end) ? __ldcg(sl + si * n_el + e) : 0.0f;
             }
         }
 #pragma unroll
@@ -693,8 +700,8 @@ __device__ __forceinline__ void reduce_tile(const KArgs& a, int rb, int warp, in
     }
 #pragma unroll
     for (int i = 0; i < kIter; ++i) {
-        const int e = lane + 32 * i;
-        if (e >= n_el) continue;
+        const int e = e_begin + lane + 32 * i;
+        if (e >= e_end) continue;
         const int token = e % a.M, row16 = e / a.M;
         const int row = rb * kBlockRows + warp * kTileRows + row16;
         if (ok && row < a.N) store_output<NS>(a, row, token, sum[i][0], sum[i][NS - 1]);
@@ -712,7 +719,7 @@ __device__ __forceinline__ void reduce_tile(const KArgs& a, int rb, int warp, in
 // together, summing them in range order.
 template <int NS, int MAXM>
 __device__ __forceinline__ void reduce_tile_em(const KArgs& a, int rb, int warp, int lane,
-                                               bool ok) {
+                                               bool ok, int e_begin, int e_end) {
     constexpr int kIter = (kTileRows * MAXM + 31) / 32;  // elements per lane at the largest M
     constexpr int kPB = 32 / (kIter * NS);                 // parts per batch (32 in flight)
     static_assert(kPB % 4 == 0, "parts are read in 16-byte vectors");
@@ -729,14 +736,14 @@ __device__ __forceinline__ void reduce_tile_em(const KArgs& a, int rb, int warp,
         float part[kIter][NS][kPB];
 #pragma unroll
         for (int i = 0; i < kIter; ++i) {
-            const int e = lane + 32 * i;
+            const int e = e_begin + lane + 32 * i;
 #pragma unroll
             for (int si = 0; si < NS; ++si) {
                 const float4* src = reinterpret_cast<const float4*>(
                     base + (size_t)(si * n_el + e) * a.part_stride + p0);
 #pragma unroll
                 for (int q = 0; q < kPB / 4; ++q) {
-                    const float4 v4 = (e < n_el && p0 + 4 * q < nparts)
+                    const float4 v4 = (e < e_end && p0 + 4 * q < nparts)
                                           ? __ldcg(src + q)
                                           : make_float4(0.f, 0.f, 0.f, 0.f);
                     part[i][si][4 * q] = v4.x;
@@ -756,20 +763,69 @@ __device__ __forceinline__ void reduce_tile_em(const KArgs& a, int rb, int warp,
     }
 #pragma unroll
     for (int i = 0; i < kIter; ++i) {
-        const int e = lane + 32 * i;
-        if (e >= n_el) continue;
+        const int e = e_begin + lane + 32 * i;
+        if (e >= e_end) continue;
         const int token = e % a.M, row16 = e / a.M;
         const int row = rb * kBlockRows + warp * kTileRows + row16;
         if (ok && row < a.N) store_output<NS>(a, row, token, sum[i][0], sum[i][NS - 1]);
     }
 }
 
+// Final sums and outputs of elements [e_begin, e_end) of (row block rb, this
+// warp's tile), every part read in range order.
 template <int NS, int NT, bool DIAG, bool EM>
-__device__ __forceinline__ void reduce_any(const KArgs& a, int rb, int warp, int lane, bool ok) {
+__device__ __forceinline__ void reduce_any(const KArgs& a, int rb, int warp, int lane, bool ok,
+                                           int e_begin, int e_end) {
     if constexpr (EM)
-        reduce_tile_em<NS, DIAG ? 2 : kElemMajorMaxM>(a, rb, warp, lane, ok);
+        reduce_tile_em<NS, DIAG ? 2 : kElemMajorMaxM>(a, rb, warp, lane, ok, e_begin, e_end);
     else
-        reduce_tile<NS, NT>(a, rb, warp, lane, ok);
+        reduce_tile<NS, NT>(a, rb, warp, lane, ok, e_begin, e_end);
+}
+
+// Cooperative finish of a split row block (the non-diagonal kernels).  The
+// ranges whose last segment lies in row block rb -- every range covering rb
+// except one whose range continues into the next row block -- are its
+// participants.  Each publishes its own partial (acquire-release add on the
+// tile's counter; the lanes' partial stores are ordered before it by the
+// caller's __syncwarp), waits (bounded) until all nparts parts are counted in,
+// and then sums and stores its own share of the tile's elements, reading every
+// part in range order -- so the results do not depend on which range arrives
+// last.  The remaining range counts its part in during its stream and never
+// reduces.  Every participant adds 1 more once it has seen the full count; the
+// one that brings the counter to nparts + participants resets it to zero for
+// the next call.  A warp that gave up a wait earlier (!ok) or whose CTA
+// aborted skips all of this; the others then give up their wait after the
+// time limit and report it.
+template <int NS, int NT, bool DIAG, bool EM>
+__device__ __forceinline__ void coop_finish(const KArgs& a, int r, int rb, int warp, int lane,
+                                            bool ok, volatile int* abort_flag) {
+    if (!ok || *abort_flag) return;
+    const long long p_lo = (long long)rb * a.CS;
+    const int r_first = range_of(a, p_lo), r_last = range_of(a, p_lo + a.CS - 1);
+    const int nparts = r_last - r_first + 1;
+    const int P = r_last - r_first + (range_start(a, r_last + 1) <= p_lo + a.CS ? 1 : 0);
+    int* cnt = a.counters + rb * kBlockTiles + warp;
+    int done = 0;
+    if (lane == 0) {
+        atom_add_acq_rel_gpu(cnt, 1);
+        done = wait_count_bounded(cnt, nparts, abort_flag, a.wait_ns) ? 1 : 0;
+        if (!done) {
+            *abort_flag = 1;
+            atomicOr(a.status, 1);
+        }
+    }
+    done = __shfl_sync(0xffffffffu, done, 0);
+    __syncwarp();  // the other lanes' part loads follow lane 0's acquire
+    if (!done) return;
+    const int n_el = kTileRows * a.M;
+    const int per = (n_el + P - 1) / P;
+    const int j = r - r_first;
+    const int e0 = min(n_el, j * per), e1 = min(n_el, e0 + per);
+    reduce_any<NS, NT, DIAG, EM>(a, rb, warp, lane, ok, e0, e1);
+    if (lane == 0) {
+        const int old = atomicAdd(cnt, 1);
+        if (old == nparts + P - 1) *cnt = 0;  // every participant has seen the full count
+    }
 }
 
 template <int NT>
@@ -1046,9 +1102,14 @@ static __device__ __noinline__ bool wait_stage_slow(uint32_t bar, uint32_t parit
 // DIAG: M <= 2 with the diagonal token layout (stage_x_diag; NVFP4 only).
 // EM: element-major split-K partials (M <= kElemMajorMaxM).
 // F8: block-scaled FP8 weights (process_chunk_f8) instead of NVFP4.
-template <int NS, int NT, bool ONE, bool DIAG, bool EM, bool F8>
+// COOP: split row blocks finished cooperatively (coop_finish) instead of by the
+// last range to arrive; a compile-time choice, since a kernel holding both
+// finishing paths runs slower than either (register pressure).
+template <int NS, int NT, bool ONE, bool DIAG, bool EM, bool F8, bool COOP>
 __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a) {
     static_assert(!(F8 && DIAG), "the diagonal token layout is for NVFP4 block scales");
+    static_assert(!(COOP && DIAG), "the diagonal kernels finish by the last range to arrive");
+    constexpr bool coop = COOP;
     constexpr int CPS = (F8 ? kF8UnitsPerStep : kUnitsPerStep) / NS;  // chunks per step
     constexpr int GB = group_bytes(NS, F8);                             // bytes per chunk
 
@@ -1138,6 +1199,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
                 for (int q = q0; q < q1 && e < kMaxEvents; q += a.CS - cb, ++rb, cb = 0) {
                     const int seg_n = q1 - q < a.CS - cb ? q1 - q : a.CS - cb;
                     if (cb == 0 && seg_n == a.CS) continue;  // whole row block: stored directly
+                    if (coop && q + seg_n == q1) continue;   // last segment: coop_finish
                     if (!mbar_wait_bounded(seg_done0 + 8u * e, 0, abort_flag, a.wait_ns)) {
                         *abort_flag = 1;
                         atomicOr(a.status, 1);
@@ -1275,16 +1337,23 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
                             acc[si][nt][e] = 0.0f;
                         }
             }
+            const bool coop_last = coop && q + seg_n == q1;
             const int old = finish_segment<NS, NT, DIAG, EM>(a, hi, lo, unscale, r, q0, rb,
                                                              cb + seg_n - 1, warp, lane, ok, evt,
-                                                             seg_done0);
-            if (old != -1) {
+                                                             seg_done0, coop_last);
+            if constexpr (COOP) {
+                if (old == kSegCoop)
+                    coop_finish<NS, NT, DIAG, EM>(a, r, rb, warp, lane, ok, abort_flag);
+                else if (old != -1)
+                    ++evt;  // counted in by the publisher or this warp; a participant reduces
+            } else if (old != -1) {
                 ++evt;
                 if (n_pending == kMaxPending) {  // resolve the oldest now
                     const int o = pending_old_value(a, pend.template old<0>(), warp, pub_done0,
                                                     pub_old, abort_flag);
                     if (resolve_tile(a, pend.template rb<0>(), warp, lane, o))
-                        reduce_any<NS, NT, DIAG, EM>(a, pend.template rb<0>(), warp, lane, ok);
+                        reduce_any<NS, NT, DIAG, EM>(a, pend.template rb<0>(), warp, lane, ok, 0,
+                                                     kTileRows * a.M);
                     pend.pop_front();
                     --n_pending;
                 }
@@ -1296,7 +1365,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
     // resolve what is still pending, oldest first
     auto resolve = [&](int rbv, int oldv) {
         const int o = pending_old_value(a, oldv, warp, pub_done0, pub_old, abort_flag);
-        if (resolve_tile(a, rbv, warp, lane, o)) reduce_any<NS, NT, DIAG, EM>(a, rbv, warp, lane, ok);
+        if (resolve_tile(a, rbv, warp, lane, o))
+            reduce_any<NS, NT, DIAG, EM>(a, rbv, warp, lane, ok, 0, kTileRows * a.M);
     };
     if (n_pending > 0) resolve(pend.template rb<0>(), pend.template old<0>());
     if (n_pending > 1) resolve(pend.template rb<1>(), pend.template old<1>());
@@ -1304,14 +1374,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
     if (n_pending > 3) resolve(pend.template rb<3>(), pend.template old<3>());
 }
 
-template <int NS, int NT, bool ONE, bool DIAG, bool EM, bool F8>
+template <int NS, int NT, bool ONE, bool DIAG, bool EM, bool F8, bool COOP>
 static cudaError_t launch_t(const Plan& p, const KArgs& a, cudaStream_t s) {
     // set once per device; a second thread racing here sets it again, harmlessly
     static std::atomic<bool> attr_done[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(stream_gemv_kernel<NS, NT, ONE, DIAG, EM, F8>,
+        cudaError_t e = cudaFuncSetAttribute(stream_gemv_kernel<NS, NT, ONE, DIAG, EM, F8, COOP>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
@@ -1326,11 +1396,20 @@ static cudaError_t launch_t(const Plan& p, const KArgs& a, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, stream_gemv_kernel<NS, NT, ONE, DIAG, EM, F8>, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, stream_gemv_kernel<NS, NT, ONE, DIAG, EM, F8, COOP>, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
+
+// Whether a launch finishes split row blocks cooperatively (the COOP kernels).  It pays where the
+// final reduction is heavy -- the gate/up kernel's activation epilogue, or
+// many parts per row block -- and M >= 3 (one or two token rows leave too
+// little to share).  It needs one range per CTA: a CTA that waits at the end of
+// each of several ranges would tie every CTA's progress to its neighbours'.
+static bool use_coop(const Plan& p, int M) {
+    return p.R == p.grid && M >= 3 && (p.NS == 2 || p.R >= 4 * p.RB);
+}
 
 // Kernel arguments for a plan (the adapter deltas are left null).
 static KArgs make_kargs(const Plan& p, const void* x, int M, int K, const void* packed, int N,
