@@ -586,6 +586,42 @@ def run_sweep(args, ffi, synth, dev, timer, sampler, layers, H, I, peak):
     res[f"ffn_{H}x{I}_lora_gate_up_down"] = lr
     torch.cuda.empty_cache()
 
+    # the fixed-workspace entry point against the caller-workspace one: the same
+    # 48 calls per step issued eagerly from Python, timed with CUDA events on
+    # the issuing stream, after the fixed array's one-time set-up
+    na = {}
+    for M in (1, 8):
+        x = synth.activations_bf16(M, H, seed=M, device=dev)
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        ws = ffi.workspace(ffi.ffn_swiglu_nvfp4_workspace_bytes(M, H, I), dev)
+        entry = {}
+        for name, call in (("workspace", lambda l: ffi.ffn_swiglu_nvfp4(
+                               x, l[0], l[1], l[2], l[3], l[4], I, 0, ws=ws, out=out)),
+                           ("noalloc", lambda l: ffi.ffn_swiglu_nvfp4_noalloc(
+                               x, l[0], l[1], l[2], l[3], l[4], I, 0, out=out))):
+            st = torch.cuda.Stream(device=dev)
+            with torch.cuda.stream(st):
+                for _ in range(2):  # warm-up (includes the fixed array's set-up)
+                    for lyr in layers:
+                        call(lyr)
+                st.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                w0 = time.time()
+                e0.record(st)
+                for _ in range(reps):
+                    for lyr in layers:
+                        call(lyr)
+                e1.record(st)
+                e1.synchronize()
+                sampler.mark(w0, time.time())
+            t = e0.elapsed_time(e1) * 1e-3 / (reps * len(layers))
+            launches += 2 * len(layers) * (reps + 2)
+            entry[name] = _layer_entry(t, H, I, M, peak)
+        if ffi.nvfp4_workspace_status(ws) != 0 or ffi.nvfp4_noalloc_status() != 0:
+            raise RuntimeError("device status word reports a bounded wait abandoned")
+        na[f"M{M}"] = entry
+    res[f"ffn_{H}x{I}_noalloc_vs_workspace_eager"] = na
+
     # block-scaled FP8 weights (the pages' native FP8 arm) on the headline layer
     f8 = {}
     f8_layers = build_w8a16_layers(ffi, synth, H, I, 24, dev)
