@@ -63,6 +63,7 @@ constexpr int kSmemMax = 227 * 1024;
 constexpr int kXBudget = 96 * 1024;
 constexpr int kRingBudget = 200 * 1024;
 constexpr int kMaxStages = 8;
+constexpr int kMinStages = 3;  // fewest ring stages a widened token area may leave
 // Up to this many tokens (one MMA token group) the split-K partials are
 // element-major: each output element's parts are contiguous, and the last
 // range reads them in 16-byte vectors.  With two token groups (M > 8) each
@@ -126,9 +127,22 @@ static Plan make_plan(int NS, int M, int N, int K, int num_sms, bool f8) {
     // NVFP4 with M <= 2 uses the diagonal layout: 1024 bytes per chunk for
     // both tokens.
     const bool diag = M <= 2 && !f8;
-    const int xcap_max = diag ? kXBudget / 1024 : (kXBudget - 16 * M) / (128 * M);
+    auto xcap_for = [&](int budget) {
+        return diag ? budget / 1024 : (budget - 16 * M) / (128 * M);
+    };
+    int xcap_max = xcap_for(kXBudget);
     p.grid = num_sms > 0 ? num_sms : 1;
     if (p.L < p.grid) p.grid = (int)p.L;
+    {
+        // One range per CTA saves a second staging, tail and set of partials;
+        // when the token rows of such a range just miss the budget, let them
+        // take ring space as long as kMinStages stages remain.
+        const long long need1 = ceil_div(p.L, p.grid) * p.cps < p.C ? ceil_div(p.L, p.grid) * p.cps
+                                                                     : p.C;
+        const int stage = p.cps * group_bytes(NS, f8);
+        const int wide = kSmemMax - kMiscBytes - 32 * kMaxStages - 512 - kMinStages * stage;
+        if (need1 > xcap_max && need1 <= xcap_for(wide)) xcap_max = xcap_for(wide);
+    }
     for (int rpc = 1;; ++rpc) {
         long long R = (long long)p.grid * rpc;
         if (R > p.L) R = p.L;

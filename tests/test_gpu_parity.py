@@ -375,9 +375,11 @@ def test_ffn_full_size(dev, M, act, outliers):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("M,act", [(1, ffi.NVFP4_ACT_SILU), (5, ffi.NVFP4_ACT_GELU_TANH),
-                                   (12, ffi.NVFP4_ACT_SILU)])
+                                   (12, ffi.NVFP4_ACT_SILU), (16, ffi.NVFP4_ACT_GELU_TANH)])
 def test_ffn_large_dense_shape(dev, M, act):
-    """The large dense FFN sweep's layer shape, H=5376, I=21504."""
+    """The large dense FFN sweep's layer shape, H=5376, I=21504.  At M=16 the
+    down kernel's token rows take ring space (three stages) so that each CTA
+    keeps one range."""
     run_ffn_case(dev, 5376, 21504, M, act, outliers=0.0, seed=100 + M)
 
 
