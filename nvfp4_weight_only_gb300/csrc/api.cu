@@ -321,16 +321,16 @@ nvfp4_status ffn_swiglu_nvfp4_lora(const void* x, int M, int H, int I, const voi
                                 status, counters, w + l.ffn.dual_off, l.ffn.dual_bytes, sms, true,
                                 stream, np > 0 ? deltas : nullptr);
     if (e != cudaSuccess) return NVFP4_ERR_CUDA;
-    void* xad = w + l.xa_d;
-    if (down_a) {  // A_down h, ahead of the down kernel
-        e = nvf::launch_lora_xa(h, M, I, &down_a, &xad, 1, rank, stream);
-        if (e != cudaSuccess) return NVFP4_ERR_CUDA;
-    }
+    // The down kernel follows the gate/up kernel directly, so that it streams
+    // its weights while the gate/up kernel finishes; A_down h comes after it.
     e = nvf::launch_stream_gemv(1, h, M, I, down_packed, H, down_scale2, down_scale2, 0, out,
                                 status, counters + l.ffn.down_cnt_off / sizeof(int),
                                 w + l.ffn.down_off, l.ffn.down_bytes, sms, true, stream);
     if (e != cudaSuccess) return NVFP4_ERR_CUDA;
-    if (down_a) {  // out = bf16(out + B_down xa_down)
+    void* xad = w + l.xa_d;
+    if (down_a) {  // out = bf16(out + B_down bf16(A_down h))
+        e = nvf::launch_lora_xa(h, M, I, &down_a, &xad, 1, rank, stream);
+        if (e != cudaSuccess) return NVFP4_ERR_CUDA;
         const void* xac = xad;
         e = nvf::launch_lora_delta(&xac, I, &down_b, &out, 1, M, H, rank, true, stream);
         if (e != cudaSuccess) return NVFP4_ERR_CUDA;
