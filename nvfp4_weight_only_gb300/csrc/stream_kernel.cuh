@@ -1416,13 +1416,21 @@ static cudaError_t launch_t(const Plan& p, const KArgs& a, cudaStream_t s) {
 }
 
 
-// Whether a launch finishes split row blocks cooperatively (the COOP kernels).  It pays where the
-// final reduction is heavy -- the gate/up kernel's activation epilogue, or
-// many parts per row block -- and M >= 3 (one or two token rows leave too
-// little to share).  It needs one range per CTA: a CTA that waits at the end of
-// each of several ranges would tie every CTA's progress to its neighbours'.
+// Whether a launch finishes split row blocks cooperatively (the COOP kernels).
+// It pays where the final reduction is heavy; below that its extra round trip
+// (publish, wait for the full count, then load) costs more than the shared
+// work saves.  Measured on GB300 (5120 x 17408 and 4096 x 12288 layers): the
+// gate/up kernel, whose epilogue evaluates the activation, gains from M = 7;
+// a single projection gains from M = 4 when its row blocks are split into at
+// least four parts and its ranges are at least four steps long (a 4096 x
+// 4096 projection, two steps per range, lost 1 us at M = 4), and from M = 9
+// (two token tiles) at any split.  It needs
+// one range per CTA: a CTA that waits at the end of each of several ranges
+// would tie every CTA's progress to its neighbours'.
 static bool use_coop(const Plan& p, int M) {
-    return p.R == p.grid && M >= 3 && (p.NS == 2 || p.R >= 4 * p.RB);
+    if (p.R != p.grid) return false;
+    if (p.NS == 2) return M >= 7;
+    return M >= 9 || (M >= 4 && p.R >= 4 * p.RB && p.Pmax >= 4);
 }
 
 // Kernel arguments for a plan (the adapter deltas are left null).
