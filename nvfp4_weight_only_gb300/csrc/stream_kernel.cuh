@@ -16,7 +16,7 @@
 //   * weights stream through a ring of shared-memory stages filled by the
 //     bulk-copy (TMA) engine: one lane of a producer warpgroup issues every
 //     copy, a "full" mbarrier per stage completes on the copy's bytes and an
-//     "empty" mbarrier on the 16 consumer warps' release, so the consumers
+//     "empty" mbarrier on the 512 consumer lanes' release, so the consumers
 //     never issue copies and never wait for one another;
 //   * per k16 block a warp turns its 4 code bytes into exact f16 A fragments
 //     (one cvt per E2M1 pair), runs mma.sync m16n8k16 against the token rows
@@ -25,8 +25,10 @@
 //     f16 range), and applies the two E4M3 row scales to the fp32 block sums;
 //   * work = (row block, step of chunks) in row-major order, split into equal
 //     contiguous ranges; a row block whose K range spans several ranges is
-//     finished by the last range to arrive (atomic counter), which sums the
-//     fp32 partial slots in range order, so results are deterministic.
+//     finished either by the last range to arrive (atomic counter) or, where
+//     the final sums are heavy (use_coop), by all ranges that end in it, each
+//     taking a share of the outputs (coop_finish).  Either way every output
+//     sums the fp32 partials in range order, so results are deterministic.
 //
 // The block-scaled FP8 weights of the dense-FFN page's native FP8 arm
 // (DenseFfnWeightsFp8: E4M3 bytes [N, K] with an FP32 scale per 128 x 128
