@@ -70,3 +70,35 @@ def test_abandoned_wait_reports_timeout_then_next_call_is_correct(dev, M):
     y = ffi.nvfp4_gemv(ffi.ffn_hidden_view(ws, M, I).contiguous(), dn, q[2][2], H, ws=ws_g)
     assert torch.equal(y, out)
     assert ffi.nvfp4_workspace_status(ws_g) == 0
+
+
+@pytest.mark.parametrize("M", [1, 8, 12])
+def test_fp8_abandoned_wait_reports_timeout_then_next_call_is_correct(dev, M):
+    """The block-scaled FP8 kernels share the bounded waits: the same switch
+    makes their first wait run out, the status reports it, and after a
+    zero-fill the next call on the workspace is correct."""
+    H, I = 512, 1536
+    proj = [synth.fp8_weights(I, H, seed=71), synth.fp8_weights(I, H, seed=72),
+            synth.fp8_weights(H, I, seed=73)]
+    gu = ffi.w8a16_repack_gate_up(*(t.to(dev) for t in (*proj[0], *proj[1])))
+    dn = ffi.w8a16_repack(proj[2][0].to(dev), proj[2][1].to(dev))
+    q = [(c.numpy(), g.numpy()) for c, g in proj]
+    x = synth.activations_bf16(M, H, seed=M, outlier_frac=0.01)
+    xd = x.to(dev)
+    L = ffi.load()
+    ws = ffi.workspace(L.ffn_swiglu_w8a16_workspace_bytes(M, H, I), dev)
+    assert L.nvfp4_testing_inject_stall(1, WAIT_NS) == 0
+    try:
+        ffi.ffn_swiglu_w8a16(xd, gu, dn, I, ws=ws)
+        assert ffi.nvfp4_workspace_status(ws) == TIMEOUT
+    finally:
+        assert L.nvfp4_testing_inject_stall(0, 0) == 0
+    assert ffi.nvfp4_workspace_status(ws) == 0  # read-and-clear
+    ffi.nvfp4_workspace_init(ws)
+    out = ffi.ffn_swiglu_w8a16(xd, gu, dn, I, ws=ws)
+    torch.cuda.synchronize()
+    assert ffi.nvfp4_workspace_status(ws) == 0
+    xb = synth.bf16_bits(x)
+    h_bits = synth.bf16_bits(ffi.ffn_hidden_view(ws, M, I))
+    pc.check_hidden_fp8(h_bits, xb, q[0], q[1], oracle.ACT_SILU, f"fp8 h after timeout M={M}")
+    pc.check_gemv_fp8(synth.bf16_bits(out), h_bits, q[2], f"fp8 out after timeout M={M}")
