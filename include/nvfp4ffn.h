@@ -7,8 +7,8 @@
  *
  * What the calls restate (Atlas engine pages):
  *  - "spark_model/layers/dense_ffn.rs", module doc comment: the dense SwiGLU
- *    FFN, gate = gate_proj(x), up = up_proj(x), out = down_proj(SiLU(gate)*up),
- *    decoded with the weights dequantised inside the dot product.
+ *    FFN, the gated product of the gate and up projections of x fed to the
+ *    down projection, with the weights dequantised inside the dot product.
  *  - same page, doc comment of DenseFfnLayer::ensure_int8_weight: an NVFP4
  *    projection is packed E2M1 codes [N, K/2], one E4M3 scale per 16 K
  *    elements [N, K/16], and one FP32 `weight_scale_2` per tensor.

@@ -11,8 +11,9 @@
  *  - "spark_model/layers/dense_ffn.rs", module doc comment: the FFN is
  *    out = down_proj(act(gate_proj(x)) * up_proj(x)).
  *  - same page, doc comment of DenseFfnLayer::ensure_int8_weight: an NVFP4
- *    projection is `weight` = packed E2M1 [N, K/2], `weight_scale` = one E4M3
- *    per 16 K elements [N, K/16], `weight_scale_2` = one FP32 per tensor.
+ *    projection holds E2M1 codes two to a byte ([N, K/2], `weight`), an E4M3
+ *    scale for every 16 K elements ([N, K/16], `weight_scale`) and a single
+ *    FP32 scale for the tensor (`weight_scale_2`).
  *  - same page, DenseFfnLayer::forward (split-SiLU branch): gate and up are
  *    written as BF16 buffers, the act*up product overwrites gate as BF16, the
  *    down GEMV reads that BF16 vector.
