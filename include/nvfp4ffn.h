@@ -2,8 +2,12 @@
  * nvfp4ffn.h -- C ABI of libnvfp4ffn.so: NVFP4 weight-only SwiGLU FFN decode
  * on one NVIDIA GB300 (sm_103a).
  *
- *   out[M, H] = down( act( gate(x) ) * up(x) ),   M = 1..16,
+ *   out[M, H] = down( act( gate(x) ) * up(x) ),   M = 1..16 per kernel pass
+ *   (up to 64 rows per call, in passes of 16),
  *   x, out BF16;  gate [I, H], up [I, H], down [H, I] NVFP4;  act = SiLU | GeLU-tanh.
+ *
+ * Beside it: a LoRA delta overlay on the same FFN, and the FFN and GEMV on
+ * block-scaled FP8 weights (the w8a16 calls near the end of this header).
  *
  * What the calls restate (Atlas engine pages):
  *  - "spark_model/layers/dense_ffn.rs", module doc comment: the dense SwiGLU
@@ -32,6 +36,8 @@
  *    through cudaGetLastError().
  *  - BF16 tensors are row-major with a row stride equal to their width.
  *  - Device pointers must be 16-byte aligned.
+ *  - Every GEMV/FFN kernel reads its weights exactly once per call and sums
+ *    split-K partials in a fixed order, so results are bit-reproducible.
  *  - The GEMV/FFN kernels use programmatic dependent launch: they may start
  *    while the preceding kernel on `stream` is still finishing and begin
  *    streaming their (repacked) weights at once; they read x and write every
