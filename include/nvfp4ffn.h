@@ -36,7 +36,7 @@
  *    through cudaGetLastError().
  *  - BF16 tensors are row-major with a row stride equal to their width.
  *  - Device pointers must be 16-byte aligned.
- *  - Every GEMV/FFN kernel reads its weights exactly once per call and sums
+ *  - Every GEMV/FFN pass (up to 16 rows) reads its weights once and sums
  *    split-K partials in a fixed order, so results are bit-reproducible.
  *  - The GEMV/FFN kernels use programmatic dependent launch: they may start
  *    while the preceding kernel on `stream` is still finishing and begin
