@@ -38,13 +38,14 @@
  *  - Device pointers must be 16-byte aligned.
  *  - Every GEMV/FFN pass (up to 16 rows) reads its weights once and sums
  *    split-K partials in a fixed order, so results are bit-reproducible.
- *  - The GEMV/FFN kernels use programmatic dependent launch: they may start
- *    while the preceding kernel on `stream` is still finishing and begin
- *    streaming their (repacked) weights at once; they read x and write every
- *    output only after that kernel has completed.  So the weight buffers must
- *    not be written by the kernel issued immediately before the call on the
- *    same stream.  This library's quantise and repack calls are safe
- *    predecessors (their blocks fence their stores before exiting).
+ *  - The GEMV/FFN and LoRA kernels use programmatic dependent launch: they
+ *    may start while the preceding kernel on `stream` is still finishing and
+ *    begin reading their (repacked) weights or adapter matrices at once; they
+ *    read x and write every output only after that kernel has completed.  So
+ *    the weight and adapter buffers must not be written by the kernel issued
+ *    immediately before the call on the same stream.  This library's
+ *    quantise and repack calls are safe predecessors (their blocks fence
+ *    their stores before exiting).
  */
 #ifndef NVFP4FFN_H
 #define NVFP4FFN_H

@@ -11,7 +11,10 @@
 // Both are small next to the FFN's weight stream (r rows of A, r columns of
 // B), so what costs time is latency: the K sum is cut into slices that each
 // CTA covers with one vector load per thread, and every thread issues all of
-// its loads before the first multiply.  Sums run in a fixed order, so results
+// its loads before the first multiply.  Both kernels are launched as
+// programmatic dependents: they load their adapter matrix (never written by
+// the kernel before them) before waiting for that kernel, and read v, the
+// partials and the base only after it.  Sums run in a fixed order, so results
 // are deterministic.
 #include <cuda_bf16.h>
 
@@ -73,11 +76,16 @@ __global__ void __launch_bounds__(kLoraThreads) lora_xa_partial_kernel(const Lor
     const int v1 = min(kv, v0 + per);
     const __nv_bfloat16* A = p ? a.A[1] : a.A[0];  // no dynamic index into the parameters
     const Vec* arow = reinterpret_cast<const Vec*>(A + (size_t)j * a.K);
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int i0 = v0 + tid;
+    Vec w0{};
+    if (i0 < v1) w0 = arow[i0];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     float acc[kLoraMaxM];
 #pragma unroll
     for (int m = 0; m < kLoraMaxM; ++m) acc[m] = 0.0f;
-    for (int i = v0 + tid; i < v1; i += kLoraThreads) {
-        const Vec w = arow[i];
+    for (int i = i0; i < v1; i += kLoraThreads) {
+        const Vec w = i == i0 ? w0 : arow[i];
         Vec xv[kLoraMaxM];
 #pragma unroll
         for (int m = 0; m < kLoraMaxM; ++m)
@@ -112,16 +120,35 @@ struct LoraDeltaArgs {
     int M, N, r, split, add;
 };
 
-// One thread per output row n.  The block first completes xa = bf16(sum of the
-// slice partials, in slice order) into shared memory; each thread then loads
-// its whole B row before multiplying, forms d = bf16(sum_j B[n][j] xa[m][j])
-// for every m and stores it (add == 0) or adds it to the base as
-// bf16(base + d).  A bf16 plus a bf16 is exact in fp32 whenever the smaller
-// term can move the rounding, so one rounding of the fp32 sum is the bf16
-// rounding of the exact sum.
+// One thread per output row n.  Each thread loads its whole B row (r % 8 == 0)
+// before the wait on the preceding kernel, and its base values right after
+// it; the block meanwhile completes xa = bf16(sum of the slice partials, in
+// slice order) into shared memory.  The thread then forms
+// d = bf16(sum_j B[n][j] xa[m][j]) for every m and stores it (add == 0) or
+// adds it to the base as bf16(base + d).  A bf16 plus a bf16 is exact in fp32
+// whenever the smaller term can move the rounding, so one rounding of the
+// fp32 sum is the bf16 rounding of the exact sum.
 template <bool kVec>
 __global__ void __launch_bounds__(kLoraThreads) lora_delta_kernel(const LoraDeltaArgs a) {
     const int p = blockIdx.y;
+    const int n = blockIdx.x * kLoraThreads + threadIdx.x;
+    const bool live = n < a.N;
+    const __nv_bfloat16* brow = (p ? a.B[1] : a.B[0]) + (size_t)(live ? n : 0) * a.r;
+    __nv_bfloat16* const ocol = (p ? a.out[1] : a.out[0]) + n;
+    constexpr int kMaxV = kLoraMaxRank / 8;
+    uint4 bv[kMaxV];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if constexpr (kVec) {  // r % 8 == 0: at most 8 16-byte loads
+        const int nv = a.r / 8;
+#pragma unroll
+        for (int c = 0; c < kMaxV; ++c)
+            if (live && c < nv) bv[c] = reinterpret_cast<const uint4*>(brow)[c];
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    float base[kLoraMaxM];
+#pragma unroll
+    for (int m = 0; m < kLoraMaxM; ++m)
+        base[m] = live && a.add && m < a.M ? __bfloat162float(ocol[(size_t)m * a.N]) : 0.0f;
     __shared__ float xs[kLoraMaxM * kLoraMaxRank];  // [m][j]
     for (int i = threadIdx.x; i < a.M * a.r; i += kLoraThreads) {
         const int m = i / a.r, j = i - m * a.r;
@@ -131,19 +158,12 @@ __global__ void __launch_bounds__(kLoraThreads) lora_delta_kernel(const LoraDelt
         xs[i] = __bfloat162float(__float2bfloat16_rn(t));
     }
     __syncthreads();
-    const int n = blockIdx.x * kLoraThreads + threadIdx.x;
-    if (n >= a.N) return;
+    if (!live) return;
     float acc[kLoraMaxM];
 #pragma unroll
     for (int m = 0; m < kLoraMaxM; ++m) acc[m] = 0.0f;
-    const __nv_bfloat16* brow = (p ? a.B[1] : a.B[0]) + (size_t)n * a.r;
-    if (kVec) {  // r % 8 == 0: at most 8 16-byte loads, all issued first
-        constexpr int kMaxV = kLoraMaxRank / 8;
+    if constexpr (kVec) {
         const int nv = a.r / 8;
-        uint4 bv[kMaxV];
-#pragma unroll
-        for (int c = 0; c < kMaxV; ++c)
-            if (c < nv) bv[c] = reinterpret_cast<const uint4*>(brow)[c];
 #pragma unroll
         for (int c = 0; c < kMaxV; ++c) {
             if (c < nv) {
@@ -160,7 +180,7 @@ __global__ void __launch_bounds__(kLoraThreads) lora_delta_kernel(const LoraDelt
             }
         }
     } else {
-#pragma unroll 8
+#pragma unroll 4
         for (int j = 0; j < a.r; ++j) {
             const float bj = __bfloat162float(brow[j]);
 #pragma unroll
@@ -172,10 +192,27 @@ __global__ void __launch_bounds__(kLoraThreads) lora_delta_kernel(const LoraDelt
     for (int m = 0; m < kLoraMaxM; ++m) {
         if (m < a.M) {
             const __nv_bfloat16 d = __float2bfloat16_rn(acc[m]);
-            __nv_bfloat16* o = (p ? a.out[1] : a.out[0]) + (size_t)m * a.N + n;
-            *o = a.add ? __float2bfloat16_rn(__bfloat162float(*o) + __bfloat162float(d)) : d;
+            ocol[(size_t)m * a.N] = a.add ? __float2bfloat16_rn(base[m] + __bfloat162float(d)) : d;
         }
     }
+}
+
+// A launch that may begin while the preceding kernel on the stream finishes
+// (programmatic stream serialisation); the kernel orders itself after that
+// kernel with griddepcontrol.wait.
+template <typename Args>
+cudaError_t launch_dependent(void (*kernel)(Args), dim3 grid, cudaStream_t s, const Args& a) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kLoraThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 cudaError_t launch_lora_xa(const void* v, int M, int K, const void* const* A, void* const* part,
@@ -193,11 +230,8 @@ cudaError_t launch_lora_xa(const void* v, int M, int K, const void* const* A, vo
     a.K = K;
     a.split = lora_split(K);
     const dim3 grid(a.split, r, pairs);
-    if (K % 8 == 0)
-        lora_xa_partial_kernel<uint4><<<grid, kLoraThreads, 0, s>>>(a);
-    else
-        lora_xa_partial_kernel<uint32_t><<<grid, kLoraThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return K % 8 == 0 ? launch_dependent(lora_xa_partial_kernel<uint4>, grid, s, a)
+                      : launch_dependent(lora_xa_partial_kernel<uint32_t>, grid, s, a);
 }
 
 cudaError_t launch_lora_delta(const void* const* part, int K, const void* const* B,
@@ -218,11 +252,8 @@ cudaError_t launch_lora_delta(const void* const* part, int K, const void* const*
     a.split = lora_split(K);
     a.add = add ? 1 : 0;
     const dim3 grid((N + kLoraThreads - 1) / kLoraThreads, pairs);
-    if (r % 8 == 0)
-        lora_delta_kernel<true><<<grid, kLoraThreads, 0, s>>>(a);
-    else
-        lora_delta_kernel<false><<<grid, kLoraThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return r % 8 == 0 ? launch_dependent(lora_delta_kernel<true>, grid, s, a)
+                      : launch_dependent(lora_delta_kernel<false>, grid, s, a);
 }
 
 }  // namespace nvf
