@@ -420,6 +420,7 @@ __device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float*
     const int per_token = nx * 8;  // 16-byte groups of 8 k per token
     const int stride = wpt * 32;
     float mx_local = 0.0f;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (m < a.M) {
         uint8_t* row = xs + m * a.x_stride;
         // A lane's groups go in rounds of kLoads: all loads of a round are in
@@ -490,14 +491,15 @@ static __device__ void stage_x_diag(const KArgs& a, uint8_t* xs, int c_start, in
     constexpr int kLoads = 2;  // 64 chunks of 8 groups over 256 lanes (M = 2)
     const bool in_regs = per_token <= kLoads * stride;
     float mx_local = 0.0f;
+    for (int i = tid; i < nx * 64; i += kConsumerThreads)  // before the grid wait
+        reinterpret_cast<uint4*>(xs)[i] = make_uint4(0u, 0u, 0u, 0u);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     uint4 v[kLoads];
 #pragma unroll
     for (int u = 0; u < kLoads; ++u) {
         const int q = q0 + u * stride;
         v[u] = q < per_token ? load_x_group(a, m, c_start, q) : make_uint4(0u, 0u, 0u, 0u);
     }
-    for (int i = tid; i < nx * 64; i += kConsumerThreads)  // overlaps the loads
-        reinterpret_cast<uint4*>(xs)[i] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int u = 0; u < kLoads; ++u) track_amax(mx_local, v[u]);
     for (int q = q0 + kLoads * stride; q < per_token; q += stride)  // beyond the registers
@@ -1233,7 +1235,6 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
         return;
     }
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     // The ring as seen by this lane: the offset of the current stage, its
     // "full" barrier (its "empty" barrier lies bar_gap further) and phase, and
     // the lane's code and scale addresses in stage 0.
