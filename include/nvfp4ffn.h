@@ -46,6 +46,15 @@
  *    immediately before the call on the same stream.  This library's
  *    quantise and repack calls are safe predecessors (their blocks fence
  *    their stores before exiting).
+ *  - The GEMV/FFN kernels launch one block per SM.  With 4 or more token rows
+ *    a launch may finish its split row blocks cooperatively: its blocks then
+ *    wait for one another, which assumes that every block of the launch can
+ *    be resident at once.  Two such calls overlapping on the GPU (issued on
+ *    different streams or from different threads or processes sharing the
+ *    SMs) can each hold SMs that the other's blocks need; their waits then
+ *    give up after about a second and the call reports NVFP4_ERR_TIMEOUT
+ *    (nvfp4_workspace_status).  Issue the calls for one device on one stream,
+ *    or order the streams with events.
  */
 #ifndef NVFP4FFN_H
 #define NVFP4FFN_H
