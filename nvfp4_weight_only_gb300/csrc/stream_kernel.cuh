@@ -407,8 +407,10 @@ __device__ __forceinline__ uint4 load_x_group(const KArgs& a, int m, int c_start
 // f16, which is exact for every bf16 value within 2^-24 of the row's amax.
 // (The scattered 4-byte stores conflict on banks; issued before the barrier
 // they hide behind the other warps' loads, and the conversion pass is
-// conflict-free 16-byte accesses.)  amax_u[0..15] is zero on entry and left
-// zero.
+// conflict-free 16-byte accesses.)  The consumers wait for the preceding grid
+// (griddepcontrol.wait) only here, just before the first token load, so that
+// their set-up overlaps that grid's tail.  amax_u[0..15] is zero on entry and
+// left zero.
 template <int NT>
 __device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float* tok_unscale,
                         unsigned* amax_u) {
@@ -477,9 +479,9 @@ __device__ void stage_x(const KArgs& a, uint8_t* xs, int c_start, int nx, float*
 // 1024 bytes at ci*1024 hold, for lane L = 4g + t, the B registers of the four
 // MMAs: bytes h*512 + 16L + 4r (h = j/2, r = 2(j%2) + b) are the pair
 // (x[m][16j + 2t + 8b], +1) when g = 2j + m with m < M, and zero otherwise.
-// As stage_x: the loads are issued first, the area is zero-filled while they
-// are in flight, and after the amax barrier each lane converts its groups and
-// writes their words over the zeros.
+// The area is zero-filled before the wait for the preceding grid; then, as in
+// stage_x, the loads are issued together, and after the amax barrier each
+// lane converts its groups and writes their words over the zeros.
 static __device__ void stage_x_diag(const KArgs& a, uint8_t* xs, int c_start, int nx, float* tok_unscale,
                              unsigned* amax_u) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1235,6 +1237,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
         return;
     }
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
+    // (The consumers wait for the preceding grid in the token staging, just
+    // before the first token load.)
     // The ring as seen by this lane: the offset of the current stage, its
     // "full" barrier (its "empty" barrier lies bar_gap further) and phase, and
     // the lane's code and scale addresses in stage 0.
