@@ -10,12 +10,13 @@
 //
 // Both are small next to the FFN's weight stream (r rows of A, r columns of
 // B), so what costs time is latency: the K sum is cut into slices that each
-// CTA covers with one vector load per thread, and every thread issues all of
-// its loads before the first multiply.  Both kernels are launched as
-// programmatic dependents: they load their adapter matrix (never written by
-// the kernel before them) before waiting for that kernel, and read v, the
-// partials and the base only after it.  Sums run in a fixed order, so results
-// are deterministic.
+// CTA covers with one vector load per thread, every thread issues its loads
+// before the first multiply, and code that each thread runs once is kept
+// small (its first execution fetches every instruction line from L2).  Both
+// kernels are launched as programmatic dependents: they load their adapter
+// matrix (never written by the kernel before them) before waiting for that
+// kernel, and read v, the partials and the base only after it.  Sums run in a
+// fixed order, so results are deterministic.
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -120,10 +121,63 @@ struct LoraDeltaArgs {
     int M, N, r, split, add;
 };
 
+// xs[m*r + j] = bf16(sum of part[j][s][m] over the slices s, in slice order),
+// read from L2; the loads of one sum go out eight at a time.
+__device__ __forceinline__ void fill_xa(const float* part, int M, int r, int split, float* xs) {
+    for (int i = threadIdx.x; i < M * r; i += kLoraThreads) {
+        const int m = i / r, j = i - m * r;
+        const float* q = part + (size_t)j * split * M + m;
+        float t = 0.0f;
+#pragma unroll 8
+        for (int sl = 0; sl < split; ++sl) t += __ldcg(q + (size_t)sl * M);
+        xs[i] = __bfloat162float(__float2bfloat16_rn(t));
+    }
+}
+
+// Row n of every token's delta: d = bf16(sum_j B[n][j] xa[m][j]), stored at
+// ocol[m*N] (add false) or added to the base there as bf16(base + d).  bv: the
+// row of B (r % 8 == 0), else brow is read.  base0: token 0's base, loaded by
+// the caller ahead of time.  The token loop stays rolled: this code runs once
+// per row, so its size, not its issue count, is what costs (every first
+// execution of an instruction line is a fetch from L2).
+template <bool kVec>
+__device__ __forceinline__ void delta_row(const uint4 (&bv)[kLoraMaxRank / 8],
+                                          const __nv_bfloat16* brow, const float* xs, int M,
+                                          int r, int N, bool add, float base0,
+                                          __nv_bfloat16* ocol) {
+    for (int m = 0; m < M; ++m) {
+        __nv_bfloat16* const o = ocol + (size_t)m * N;
+        const float base = !add ? 0.0f : m == 0 ? base0 : __bfloat162float(*o);
+        const float* xm = xs + m * r;
+        float acc = 0.0f;
+        if constexpr (kVec) {
+            const int nv = r / 8;
+#pragma unroll
+            for (int c = 0; c < kLoraMaxRank / 8; ++c) {
+                if (c < nv) {
+                    const uint32_t words[4] = {bv[c].x, bv[c].y, bv[c].z, bv[c].w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const uint32_t wd = words[e >> 1];  // element 2i in the low half
+                        const float bj =
+                            __uint_as_float((e & 1) ? (wd & 0xffff0000u) : (wd << 16));
+                        acc = fmaf(bj, xm[8 * c + e], acc);
+                    }
+                }
+            }
+        } else {
+#pragma unroll 4
+            for (int j = 0; j < r; ++j) acc = fmaf(__bfloat162float(brow[j]), xm[j], acc);
+        }
+        const __nv_bfloat16 d = __float2bfloat16_rn(acc);
+        *o = add ? __float2bfloat16_rn(base + __bfloat162float(d)) : d;
+    }
+}
+
 // One thread per output row n.  Each thread loads its whole B row (r % 8 == 0)
-// before the wait on the preceding kernel, and its base values right after
-// it; the block meanwhile completes xa = bf16(sum of the slice partials, in
-// slice order) into shared memory.  The thread then forms
+// before the wait on the preceding kernel, and token 0's base value right
+// after it; the block meanwhile completes xa = bf16(sum of the slice
+// partials, in slice order) into shared memory.  The thread then forms
 // d = bf16(sum_j B[n][j] xa[m][j]) for every m and stores it (add == 0) or
 // adds it to the base as bf16(base + d).  A bf16 plus a bf16 is exact in fp32
 // whenever the smaller term can move the rounding, so one rounding of the
@@ -145,56 +199,11 @@ __global__ void __launch_bounds__(kLoraThreads) lora_delta_kernel(const LoraDelt
             if (live && c < nv) bv[c] = reinterpret_cast<const uint4*>(brow)[c];
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    float base[kLoraMaxM];
-#pragma unroll
-    for (int m = 0; m < kLoraMaxM; ++m)
-        base[m] = live && a.add && m < a.M ? __bfloat162float(ocol[(size_t)m * a.N]) : 0.0f;
+    const float base0 = live && a.add ? __bfloat162float(ocol[0]) : 0.0f;
     __shared__ float xs[kLoraMaxM * kLoraMaxRank];  // [m][j]
-    for (int i = threadIdx.x; i < a.M * a.r; i += kLoraThreads) {
-        const int m = i / a.r, j = i - m * a.r;
-        const float* q = (p ? a.part[1] : a.part[0]) + (size_t)j * a.split * a.M + m;
-        float t = 0.0f;
-        for (int sl = 0; sl < a.split; ++sl) t += q[(size_t)sl * a.M];
-        xs[i] = __bfloat162float(__float2bfloat16_rn(t));
-    }
+    fill_xa(p ? a.part[1] : a.part[0], a.M, a.r, a.split, xs);
     __syncthreads();
-    if (!live) return;
-    float acc[kLoraMaxM];
-#pragma unroll
-    for (int m = 0; m < kLoraMaxM; ++m) acc[m] = 0.0f;
-    if constexpr (kVec) {
-        const int nv = a.r / 8;
-#pragma unroll
-        for (int c = 0; c < kMaxV; ++c) {
-            if (c < nv) {
-                const uint32_t words[4] = {bv[c].x, bv[c].y, bv[c].z, bv[c].w};
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint32_t wd = words[e >> 1];  // element 2i in the low half
-                    const float bj = __uint_as_float((e & 1) ? (wd & 0xffff0000u) : (wd << 16));
-                    const int j = 8 * c + e;
-#pragma unroll
-                    for (int m = 0; m < kLoraMaxM; ++m)
-                        if (m < a.M) acc[m] = fmaf(bj, xs[m * a.r + j], acc[m]);
-                }
-            }
-        }
-    } else {
-#pragma unroll 4
-        for (int j = 0; j < a.r; ++j) {
-            const float bj = __bfloat162float(brow[j]);
-#pragma unroll
-            for (int m = 0; m < kLoraMaxM; ++m)
-                if (m < a.M) acc[m] = fmaf(bj, xs[m * a.r + j], acc[m]);
-        }
-    }
-#pragma unroll
-    for (int m = 0; m < kLoraMaxM; ++m) {
-        if (m < a.M) {
-            const __nv_bfloat16 d = __float2bfloat16_rn(acc[m]);
-            ocol[(size_t)m * a.N] = a.add ? __float2bfloat16_rn(base[m] + __bfloat162float(d)) : d;
-        }
-    }
+    if (live) delta_row<kVec>(bv, brow, xs, a.M, a.r, a.N, a.add != 0, base0, ocol);
 }
 
 // A launch that may begin while the preceding kernel on the stream finishes
