@@ -1383,16 +1383,18 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemv_kernel(const KArgs a)
             }
         }
     }
-    // resolve what is still pending, oldest first
-    auto resolve = [&](int rbv, int oldv) {
-        const int o = pending_old_value(a, oldv, warp, pub_done0, pub_old, abort_flag);
-        if (resolve_tile(a, rbv, warp, lane, o))
-            reduce_any<NS, NT, DIAG, EM>(a, rbv, warp, lane, ok, 0, kTileRows * a.M);
-    };
-    if (n_pending > 0) resolve(pend.template rb<0>(), pend.template old<0>());
-    if (n_pending > 1) resolve(pend.template rb<1>(), pend.template old<1>());
-    if (n_pending > 2) resolve(pend.template rb<2>(), pend.template old<2>());
-    if (n_pending > 3) resolve(pend.template rb<3>(), pend.template old<3>());
+    // Resolve what is still pending, oldest first, in a rolled loop: this code
+    // runs once per kernel, so one copy of it (fewer instruction lines to
+    // fetch from L2) is what counts, not its issue count.
+#pragma unroll 1
+    for (; n_pending > 0; --n_pending) {
+        const int o = pending_old_value(a, pend.template old<0>(), warp, pub_done0, pub_old,
+                                        abort_flag);
+        if (resolve_tile(a, pend.template rb<0>(), warp, lane, o))
+            reduce_any<NS, NT, DIAG, EM>(a, pend.template rb<0>(), warp, lane, ok, 0,
+                                         kTileRows * a.M);
+        pend.pop_front();
+    }
 }
 
 template <int NS, int NT, bool ONE, bool DIAG, bool EM, bool F8, bool COOP>
